@@ -1,0 +1,356 @@
+"""Benchmark of the Kara compression step on GB300: one JSON line on stdout.
+
+A step is one kara_compress_batch over a whole batch (plan, score, select,
+compact, commit) on inputs already resident in HBM.  Default workload: the
+Qwen3-14B-shaped batch (128 sequences x 40 layers x 8 KV heads = 40960
+windows, W 1024).  `--impl reference` times the CPU oracle on the host cores
+on a bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kara|reference]
+                       [--config qwen3_14b|qwen3_4b|llama_8b|tiny]
+Multi-GPU: launched by torch.distributed.run, each rank compresses its own
+batch (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "compressed windows/sec (seq·layer·kv-head), HBM GB/s, % of roofline"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic(spec, lengths):
+    """Per-step algorithmic work: QK^T FLOPs of the scoring and minimum bytes.
+
+    FLOPs/window = 2*G*W^2*D.  Bytes/window = Q window (G*W*D*2) + K window
+    (W*D*2) read once + V rows read and K/V rows written for the o + R + B rows
+    each window keeps (o = (L - W) mod 16)."""
+    G, W, D = spec.hq // spec.hkv, spec.W, spec.d
+    per_layer_head = spec.layers * spec.hkv
+    flops = 2.0 * G * W * W * D * spec.n_seq * per_layer_head
+    score_bytes = (G * W * D * 2 + W * D * 2) * spec.n_seq * per_layer_head
+    rows = sum(((int(L) - W) % spec.block) + spec.R + spec.B for L in lengths)
+    compact_bytes = rows * per_layer_head * D * 2 * 3     # V read, K and V written (K read: in score_bytes)
+    return flops, score_bytes, compact_bytes
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        except Exception:
+            return out
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, reasons = [], set()
+        mx = None
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+        return out
+
+
+def cpu_oracle_sample(wl_dev, seqs, layers_sample):
+    """Time the oracle (as it stands) on a bounded sample: the windows of a few
+    sequences and layers of the same workload.  Returns (windows/s, seconds, threads, windows)."""
+    import oracle
+    sub = synth.host_subset(wl_dev, seqs)
+    spec = sub.spec.with_(layers=layers_sample)
+    q = sub.q[:, :layers_sample].contiguous()
+    k = sub.k[:layers_sample].contiguous()
+    v = sub.v[:layers_sample].contiguous()
+    sh = oracle.make_shape(spec.n_seq, spec.layers, spec.hq, spec.hkv, spec.d, spec.block, spec.W, spec.B,
+                           spec.K, spec.R, spec.lam, sub.bt_stride, sub.num_blocks)
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    sc = oracle.scores(sh, q, k, sub.block_table, sub.lengths, nthreads=threads)
+    _, kept = oracle.select_batch(sc, spec.K, spec.R, spec.lam, nthreads=threads)
+    st = oracle.compact(sh, k, v, sub.block_table, sub.lengths, kept, sub.fresh)[0]
+    dt = time.perf_counter() - t0
+    assert st == oracle.OK
+    nwin = spec.n_seq * spec.layers * spec.hkv
+    return nwin / dt, dt, threads, nwin
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, ws, rank):
+    """The oracle arm: each step is a bounded sample of the workload on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec = synth.SPECS[args.config]
+    seqs = list(range(min(2, spec.n_seq)))
+    layers_sample = 1
+    wl = synth.generate(spec.with_(n_seq=len(seqs), layers=layers_sample), device="cpu")
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, seqs, layers_sample)
+    times = []
+    nwin = 0
+    thr = oracle.max_threads()
+    for _ in range(args.steps):
+        rate, dt, thr, nwin = cpu_oracle_sample(wl, seqs, layers_sample)
+        times.append(dt)
+    t = statistics.median(times)
+    val = nwin / t
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "windows/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config}: oracle sample of {nwin} windows "
+                                   f"({len(seqs)} sequences x {layers_sample} layer x {spec.hkv} KV heads)"},
+            "cpu_baseline": {"value": val, "unit": "windows/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{nwin} windows of the {args.config} workload per step"},
+            "e2e": {"value": val, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kara", choices=["kara", "reference"])
+    ap.add_argument("--config", default="qwen3_14b", choices=sorted(synth.SPECS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    ws_, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws_, rank)
+        return
+
+    from decode_kv_cache_03_gb300 import build as kbuild
+    if rank == 0 or ws_ == 1:
+        kbuild.build()
+    barrier(ws_)
+    from decode_kv_cache_03_gb300 import kara
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synth.SPECS[args.config].with_(seed=synth.SPECS[args.config].seed + 97 * rank)
+    wl = synth.generate(spec, device=dev)
+    torch.cuda.synchronize()
+    c = kara.cache(wl.k, wl.v, spec.hq)
+    p = kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam)
+    lengths_h = wl.lengths.cpu()
+    nn, no, tn, to = kara.kara_plan(p, spec.block, lengths_h, wl.bt_stride)
+    bt0 = wl.block_table.clone()
+    bt = wl.block_table
+    b = kara.batch(wl.lengths, bt, wl.q)
+    fresh = wl.fresh
+    freed = torch.empty(to, dtype=torch.int32, device=dev)
+    new_len = torch.empty(spec.n_seq, dtype=torch.int32, device=dev)
+    ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(events=None):
+        bt.copy_(bt0)                      # every step compresses the same trailing windows
+        kara.kara_compress_batch(c, p, b, fresh, freed, new_len, ws, err, stream=stream, phase_events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = kara.kara_get_error(err)
+    if status != 0:
+        raise SystemExit(f"compression reported {kara.status_string(status)}")
+
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(ws_)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws_)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws_)
+    ms = total_ms / args.steps
+    score_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    select_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
+    compact_ms = statistics.mean(ev[i][3].elapsed_time(ev[i][4]) for i in range(args.steps))
+    status = kara.kara_get_error(err)
+    if status != 0:
+        raise SystemExit(f"compression reported {kara.status_string(status)}")
+
+    # end to end through the public API with host buffers: the scheduler's tables,
+    # lengths and fresh ids go up from pinned memory, the new tables, lengths,
+    # freed ids and status come back, every step
+    h_len = lengths_h.pin_memory()
+    h_bt = bt0.cpu().pin_memory()
+    h_fresh = fresh.cpu().pin_memory()
+    h_bt_out = torch.empty_like(h_bt).pin_memory()
+    h_len_out = torch.empty_like(h_len).pin_memory()
+    h_freed = torch.empty(to, dtype=torch.int32).pin_memory()
+    h_err = torch.empty(1, dtype=torch.int32).pin_memory()
+    d_len = torch.empty_like(wl.lengths)
+    d_fresh = torch.empty_like(fresh)
+    b_e2e = kara.batch(d_len, bt, wl.q)
+    e2e_steps = args.e2e_steps or args.steps
+    e2e_ms = []
+    for i in range(e2e_steps + 1):
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        d_len.copy_(h_len, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        d_fresh.copy_(h_fresh, non_blocking=True)
+        kara.kara_compress_batch(c, p, b_e2e, d_fresh, freed, new_len, ws, err, stream=stream)
+        h_bt_out.copy_(bt, non_blocking=True)
+        h_len_out.copy_(new_len, non_blocking=True)
+        h_freed.copy_(freed, non_blocking=True)
+        h_err.copy_(err, non_blocking=True)
+        a1.record(stream)
+        a1.synchronize()
+        if i > 0:
+            e2e_ms.append(a0.elapsed_time(a1))
+    assert int(h_err[0]) == 0
+    e2e_ms_v = max_over_ranks(statistics.mean(e2e_ms), ws_)
+    h2d = (h_len.numel() + h_bt.numel() + h_fresh.numel()) * 4
+    d2h = (h_bt_out.numel() + h_len_out.numel() + h_freed.numel() + 1) * 4
+
+    nwin = spec.n_windows
+    flops, score_bytes, compact_bytes = algorithmic(spec, lengths_h.tolist())
+    hbm, tf_burst, tf_sus, src = peaks()
+    achieved_tflops = flops / (score_ms * 1e-3) / 1e12
+    value = nwin * ws_ / (ms * 1e-3)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {spec.n_seq} seq x {spec.layers} layers x {spec.hkv} KV heads "
+                               f"= {nwin} windows, W {spec.W} (C {spec.C} + B {spec.B}), G {spec.G}, D {spec.d}, "
+                               f"Top-K {spec.K}, R {spec.R}",
+                   "l2": "inputs larger than L2 (Q windows and K/V pools are tens of GB per step)",
+                   "step": "block table restored by a device copy, then kara_compress_batch",
+                   "parallelism": f"dp{ws_} (independent batches per GPU)"},
+        "roofline": {"bound": "tensor", "achieved": achieved_tflops, "peak": tf_sus, "unit": "TFLOP/s",
+                     "frac": achieved_tflops / tf_sus, "traffic": None,
+                     "kernel": "window scoring (QK^T, softmax, column sums)",
+                     "peak_kind": f"{src} sustained bf16", "frac_vs_burst": achieved_tflops / tf_burst},
+        "phases_ms": {"score": score_ms, "select": select_ms, "compact_commit": compact_ms,
+                      "score_gbs": score_bytes / (score_ms * 1e-3) / 1e9,
+                      "compact_gbs": compact_bytes / (compact_ms * 1e-3) / 1e9},
+        "step_roofline": {"t_flop_ms": flops / (tf_burst * 1e12) * 1e3,
+                          "t_hbm_ms": (score_bytes + compact_bytes) / (hbm * 1e9) * 1e3,
+                          "frac": max(flops / (tf_burst * 1e12), (score_bytes + compact_bytes) / (hbm * 1e9))
+                          / (ms * 1e-3)},
+        "e2e": {"value": nwin * ws_ / (e2e_ms_v * 1e-3), "unit": "windows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": None,
+        "clocks": clocks,
+    }
+    line["gpu_launches"] = args.steps * launches_per_step()
+    if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
+        sample_seqs = list(range(min(2, spec.n_seq)))
+        bt.copy_(bt0)
+        torch.cuda.synchronize()
+        rate, dt, thr, sw = cpu_oracle_sample(wl, sample_seqs, 1)
+        line["cpu_baseline"] = {"value": rate, "unit": "windows/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{sw} windows ({len(sample_seqs)} sequences x 1 layer x "
+                                          f"{spec.hkv} KV heads) of the same workload, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def launches_per_step():
+    """Kernels of this library per kara_compress_batch: plan, score (2), select, compact, commit."""
+    return 6
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,72 @@
+// Shared device/host helpers of the Kara sm_103a library (internal header).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kara.h"
+
+namespace kara {
+
+// Per-sequence plan produced on the device by plan_kernel (summary section 3:
+// the trailing blocks of a sequence are rebuilt and the old ones released).
+struct SeqPlan {
+    int32_t L;        // cached length
+    int32_t ws;       // window start = L - W
+    int32_t p0;       // first rebuilt logical block = ws / bs
+    int32_t Lnew;     // L - C + R
+    int32_t n_new;    // fresh blocks taken
+    int32_t n_old;    // old tail blocks released
+    int32_t off_new;  // offset of this sequence's ids in the fresh list
+    int32_t off_old;  // offset in the freed list
+};
+
+// Geometry shared by every kernel of one call.
+struct Geo {
+    const uint16_t *k;    // bf16 pools as raw bits
+    const uint16_t *v;
+    int64_t layer_stride, block_stride, head_stride;
+    int32_t layers, num_blocks, hkv, hq, G, D, bs;
+    int32_t W, B, C, K, R;
+    float lambda;
+    int32_t n, bt_stride;
+    const int32_t *len;
+    const int32_t *bt;
+    const uint16_t *q;
+    int64_t nwin;         // n * layers * hkv
+};
+
+__device__ __forceinline__ void set_err(int32_t *err, int code)
+{
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Window u -> (sequence, layer, kv head).
+__device__ __forceinline__ void window_coords(const Geo &g, int64_t u, int &s, int &l, int &h)
+{
+    h = (int)(u % g.hkv);
+    l = (int)((u / g.hkv) % g.layers);
+    s = (int)(u / ((int64_t)g.hkv * g.layers));
+}
+
+// Offset (elements) of a pool row; blk must already be range-checked.
+__device__ __forceinline__ int64_t pool_off(const Geo &g, int l, int32_t blk, int h, int slot)
+{
+    return (int64_t)l * g.layer_stride + (int64_t)blk * g.block_stride + (int64_t)h * g.head_stride
+         + (int64_t)slot * g.D;
+}
+
+__host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Launchers (each returns the launch error, if any).
+cudaError_t launch_plan(const Geo &g, int64_t n_fresh, SeqPlan *plan, int32_t *err, cudaStream_t st);
+cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
+                           int64_t n_fresh, int32_t *err, cudaStream_t st);
+cudaError_t launch_commit(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int32_t *freed,
+                          int32_t *new_len, int32_t *bt, const int32_t *err, cudaStream_t st);
+cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, const float *scores,
+                          int32_t *cand, int32_t *kept, cudaStream_t st);
+size_t score_scratch_bytes(const Geo &g);
+cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
+
+}  // namespace kara

@@ -1,0 +1,267 @@
+// Host side of the C ABI: argument checks, workspace layout and the launch
+// sequence of each entry point.  No allocation, no stream synchronisation
+// (except kara_get_error).
+#include <string.h>
+
+#include "kara_common.cuh"
+
+using namespace kara;
+
+namespace {
+
+constexpr int kMaxK = 1024;
+constexpr int kMaxG = 8;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+kara_status check_params(const kara_params *p)
+{
+    if (!p) return KARA_EINVAL;
+    if (p->W < 64 || p->W > 2048 || p->W % 64 != 0) return KARA_EUNSUPPORTED;
+    if (p->B < 0 || p->B >= p->W) return KARA_EINVAL;
+    const int C = p->W - p->B;
+    if (p->K < 1 || p->K > C) return KARA_EINVAL;
+    if (p->K > kMaxK) return KARA_EUNSUPPORTED;
+    if (p->R < 1 || p->R > C) return KARA_EINVAL;
+    if (!(p->lambda == p->lambda)) return KARA_EINVAL;  // NaN
+    return KARA_OK;
+}
+
+kara_status check_cache(const kara_cache *c)
+{
+    if (!c || !c->k || !c->v) return KARA_EINVAL;
+    if (c->head_dim != 64 && c->head_dim != 128) return KARA_EUNSUPPORTED;
+    if (c->block_size != 16) return KARA_EUNSUPPORTED;
+    if (c->num_kv_heads < 1 || c->num_q_heads < 1 || c->num_q_heads % c->num_kv_heads != 0)
+        return KARA_EINVAL;
+    if (c->num_q_heads / c->num_kv_heads > kMaxG) return KARA_EUNSUPPORTED;
+    if (c->num_layers < 1 || c->num_blocks < 1) return KARA_EINVAL;
+    if (!aligned16(c->k) || !aligned16(c->v)) return KARA_EINVAL;
+    if (c->layer_stride % 8 || c->block_stride % 8 || c->head_stride % 8) return KARA_EINVAL;
+    if (c->layer_stride < 0 || c->block_stride < 0 || c->head_stride < 0) return KARA_EINVAL;
+    return KARA_OK;
+}
+
+kara_status make_geo(const kara_cache *c, const kara_params *p, const kara_batch *b, Geo *g)
+{
+    kara_status st = check_params(p);
+    if (st != KARA_OK) return st;
+    st = check_cache(c);
+    if (st != KARA_OK) return st;
+    if (!b || b->n < 0) return KARA_EINVAL;
+    if (b->n > 0 && (!b->len || !b->block_table || !b->q || b->bt_stride < 1)) return KARA_EINVAL;
+    if (b->q && !aligned16(b->q)) return KARA_EINVAL;
+    memset(g, 0, sizeof *g);
+    g->k = static_cast<const uint16_t *>(c->k);
+    g->v = static_cast<const uint16_t *>(c->v);
+    g->layer_stride = c->layer_stride;
+    g->block_stride = c->block_stride;
+    g->head_stride = c->head_stride;
+    g->layers = c->num_layers;
+    g->num_blocks = c->num_blocks;
+    g->hkv = c->num_kv_heads;
+    g->hq = c->num_q_heads;
+    g->G = c->num_q_heads / c->num_kv_heads;
+    g->D = c->head_dim;
+    g->bs = c->block_size;
+    g->W = p->W;
+    g->B = p->B;
+    g->C = p->W - p->B;
+    g->K = p->K;
+    g->R = p->R;
+    g->lambda = p->lambda;
+    g->n = b->n;
+    g->bt_stride = b->bt_stride;
+    g->len = b->len;
+    g->bt = b->block_table;
+    g->q = static_cast<const uint16_t *>(b->q);
+    g->nwin = (int64_t)b->n * c->num_layers * c->num_kv_heads;
+    return KARA_OK;
+}
+
+// Workspace layout of kara_compress_batch: [plan][scores][cand][kept][score scratch].
+struct WsLayout {
+    size_t plan, scores, cand, kept, scratch, total;
+};
+
+WsLayout layout(const Geo &g)
+{
+    WsLayout w;
+    size_t off = 0;
+    w.plan = off;
+    off += align256((size_t)(g.n > 0 ? g.n : 1) * sizeof(SeqPlan));
+    w.scores = off;
+    off += align256((size_t)g.nwin * g.C * sizeof(float));
+    w.cand = off;
+    off += align256((size_t)g.nwin * g.K * sizeof(int32_t));
+    w.kept = off;
+    off += align256((size_t)g.nwin * g.R * sizeof(int32_t));
+    w.scratch = off;
+    off += score_scratch_bytes(g);
+    w.total = off;
+    return w;
+}
+
+template <class T>
+T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+kara_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KARA_OK : KARA_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *kara_status_string(int status)
+{
+    switch (status) {
+        case KARA_OK: return "KARA_OK";
+        case KARA_EINVAL: return "KARA_EINVAL: argument or cached length out of range";
+        case KARA_EUNSUPPORTED: return "KARA_EUNSUPPORTED: shape outside the supported set";
+        case KARA_ENOBLOCKS: return "KARA_ENOBLOCKS: fresh-block list too short";
+        case KARA_EDUPBLOCK: return "KARA_EDUPBLOCK: duplicate block id";
+        case KARA_ECUDA: return "KARA_ECUDA: CUDA runtime error";
+        case KARA_EBADBLOCK: return "KARA_EBADBLOCK: block id outside the pool";
+        case KARA_ETIMEOUT: return "KARA_ETIMEOUT: bounded device wait ran out";
+        case KARA_EWORKSPACE: return "KARA_EWORKSPACE: workspace missing or too small";
+        default: return "KARA_UNKNOWN";
+    }
+}
+
+int kara_version(void) { return 1; }
+
+kara_status kara_plan(const kara_params *p, int32_t block_size, int32_t n, const int32_t *h_len,
+                      int32_t bt_stride, int32_t *h_n_new, int32_t *h_n_old, int64_t *h_total_new,
+                      int64_t *h_total_old)
+{
+    kara_status st = check_params(p);
+    if (st != KARA_OK) return st;
+    if (block_size < 1 || n < 0 || (n > 0 && !h_len)) return KARA_EINVAL;
+    int64_t tn = 0, to = 0;
+    for (int32_t s = 0; s < n; ++s) {
+        const int64_t L = h_len[s];
+        if (L < p->W || (L + block_size - 1) / block_size > bt_stride) return KARA_EINVAL;
+        const int64_t ws = L - p->W, p0 = ws / block_size, Lnew = ws + p->R + p->B;
+        const int32_t no = (int32_t)((L + block_size - 1) / block_size - p0);
+        const int32_t nn = (int32_t)((Lnew + block_size - 1) / block_size - p0);
+        if (h_n_new) h_n_new[s] = nn;
+        if (h_n_old) h_n_old[s] = no;
+        tn += nn;
+        to += no;
+    }
+    if (h_total_new) *h_total_new = tn;
+    if (h_total_old) *h_total_old = to;
+    return KARA_OK;
+}
+
+size_t kara_workspace_size(const kara_cache *c, const kara_params *p, int32_t n)
+{
+    if (check_params(p) != KARA_OK || check_cache(c) != KARA_OK || n < 0) return 0;
+    Geo g;
+    memset(&g, 0, sizeof g);
+    g.layers = c->num_layers;
+    g.hkv = c->num_kv_heads;
+    g.hq = c->num_q_heads;
+    g.G = c->num_q_heads / c->num_kv_heads;
+    g.D = c->head_dim;
+    g.W = p->W;
+    g.C = p->W - p->B;
+    g.K = p->K;
+    g.R = p->R;
+    g.n = n;
+    g.nwin = (int64_t)n * c->num_layers * c->num_kv_heads;
+    return layout(g).total;
+}
+
+kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_batch *b, float *scores,
+                       void *ws, size_t ws_bytes, int32_t *err, kara_stream_t stream)
+{
+    Geo g;
+    kara_status st = make_geo(c, p, b, &g);
+    if (st != KARA_OK) return st;
+    if (g.nwin == 0) return KARA_OK;
+    if (!scores || !err) return KARA_EINVAL;
+    const size_t need = score_scratch_bytes(g);
+    if (need && (!ws || ws_bytes < need)) return KARA_EWORKSPACE;
+    return cuda_status(launch_score(g, scores, ws, err, (cudaStream_t)stream));
+}
+
+kara_status kara_select(const kara_params *p, int64_t n_windows, const float *scores, int32_t *cand,
+                        int32_t *kept, kara_stream_t stream)
+{
+    kara_status st = check_params(p);
+    if (st != KARA_OK) return st;
+    if (n_windows < 0) return KARA_EINVAL;
+    if (n_windows == 0) return KARA_OK;
+    if (!scores || !kept) return KARA_EINVAL;
+    if (n_windows > 0x7fffffffLL) return KARA_EUNSUPPORTED;
+    return cuda_status(launch_select(n_windows, p->W - p->B, p->K, p->R, p->lambda, scores, cand, kept,
+                                     (cudaStream_t)stream));
+}
+
+kara_status kara_compact(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                         const int32_t *kept, const int32_t *fresh, int64_t n_fresh, int32_t *freed,
+                         int32_t *new_len, int32_t *err, void *ws, size_t ws_bytes, kara_stream_t stream)
+{
+    Geo g;
+    kara_status st = make_geo(c, p, b, &g);
+    if (st != KARA_OK) return st;
+    if (g.n == 0) return KARA_OK;
+    if (!kept || !new_len || !err || n_fresh < 0 || (n_fresh > 0 && !fresh) || !freed)
+        return KARA_EINVAL;
+    const WsLayout w = layout(g);
+    if (!ws || ws_bytes < w.plan + align256((size_t)g.n * sizeof(SeqPlan))) return KARA_EWORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    SeqPlan *plan = at<SeqPlan>(ws, w.plan);
+    cudaError_t e = launch_plan(g, n_fresh, plan, err, s);
+    if (e == cudaSuccess) e = launch_compact(g, plan, kept, fresh, n_fresh, err, s);
+    if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);
+    return cuda_status(e);
+}
+
+kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                const int32_t *fresh, int64_t n_fresh, int32_t *freed, int32_t *new_len,
+                                float *scores_out, int32_t *cand_out, int32_t *kept_out, void *ws,
+                                size_t ws_bytes, int32_t *err, kara_stream_t stream,
+                                void *const *phase_events)
+{
+    Geo g;
+    kara_status st = make_geo(c, p, b, &g);
+    if (st != KARA_OK) return st;
+    if (g.n == 0) return KARA_OK;
+    if (!new_len || !err || n_fresh < 0 || (n_fresh > 0 && !fresh) || !freed) return KARA_EINVAL;
+    if (g.nwin > 0x7fffffffLL) return KARA_EUNSUPPORTED;
+    const WsLayout w = layout(g);
+    if (!ws || ws_bytes < w.total) return KARA_EWORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    SeqPlan *plan = at<SeqPlan>(ws, w.plan);
+    float *scores = scores_out ? scores_out : at<float>(ws, w.scores);
+    int32_t *cand = cand_out ? cand_out : at<int32_t>(ws, w.cand);
+    int32_t *kept = kept_out ? kept_out : at<int32_t>(ws, w.kept);
+    auto mark = [&](int i) -> cudaError_t {
+        return phase_events ? cudaEventRecord((cudaEvent_t)phase_events[i], s) : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = launch_plan(g, n_fresh, plan, err, s);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = launch_score(g, scores, at<void>(ws, w.scratch), err, s);
+    if (e == cudaSuccess) e = mark(2);
+    if (e == cudaSuccess) e = launch_select(g.nwin, g.C, g.K, g.R, g.lambda, scores, cand, kept, s);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess) e = launch_compact(g, plan, kept, fresh, n_fresh, err, s);
+    if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);
+    if (e == cudaSuccess) e = mark(4);
+    return cuda_status(e);
+}
+
+kara_status kara_get_error(const int32_t *err, kara_stream_t stream)
+{
+    if (!err) return KARA_EINVAL;
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, err, sizeof h, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return KARA_ECUDA;
+    return (kara_status)h;
+}
+
+}  // extern "C"

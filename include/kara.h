@@ -1,0 +1,197 @@
+/*
+ * kara.h -- C ABI of the GB300 (sm_103a) library for Kara's decode-time
+ * KV-cache compression step.
+ *
+ * The method comes from "Kara: Sliding-Window KV Cache Compression for
+ * Efficient Serving of Reasoning LLMs under Memory Constraints" (arXiv
+ * 2607.01237; abstract and Section 1) and the gist.science technical summary
+ * of that paper (sections "1. Sliding-Window Bidirectional Attention
+ * Scoring", "2. Token2Chunk Module", "3. KvLLM Framework and Periodic
+ * Compression").  For every window u = (sequence s, layer l, KV head g) the
+ * step scores the W most recent tokens' keys with the queries of all W window
+ * tokens, picks Top-K candidates, expands them into chunks under a retention
+ * budget and packs the retained K/V rows into fresh paged blocks.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless their name starts with h_.
+ *   - The caller owns all memory.  No entry point allocates device memory and
+ *     none synchronises the stream, except kara_get_error, which waits for it.
+ *   - Calls are asynchronous on `stream`.  The return value is the result of
+ *     the host-side argument checks only; KARA_OK means the work was enqueued.
+ *   - Device-side failures (a length shorter than the window, a block id
+ *     outside the pool, a fresh list that is too short) are recorded in the
+ *     caller's device word `err` (int32): the first error code wins, later
+ *     ones are dropped.  The caller zeroes `err` before a step;
+ *     kara_compress_batch zeroes it itself.  Read it with kara_get_error.
+ *   - bf16 everywhere for Q, K and V; rows of head_dim elements are
+ *     contiguous and 16-byte aligned.
+ *
+ * Notation: L cached length, W window, ws = L - W, B protected buffer,
+ * C = W - B compressible keys, G = num_q_heads / num_kv_heads (query heads
+ * g*G .. g*G+G-1 belong to KV head g), D head dim, bs block size,
+ * p0 = floor(ws / bs), L' = L - C + R.
+ *
+ * Supported shapes: D in {64, 128}; block_size 16; 1 <= G <= 8;
+ * W a multiple of 64 with 64 <= W <= 2048; 1 <= K <= min(C, 1024);
+ * 1 <= R <= C.  Anything else returns KARA_EUNSUPPORTED or KARA_EINVAL.
+ */
+#ifndef KARA_H
+#define KARA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *kara_stream_t;
+
+typedef enum {
+    KARA_OK = 0,
+    KARA_EINVAL = -1,        /* an argument or a cached length is out of range */
+    KARA_EUNSUPPORTED = -2,  /* a shape outside the supported set above */
+    KARA_ENOBLOCKS = -3,     /* the fresh-block list is shorter than the plan needs */
+    KARA_EDUPBLOCK = -4,     /* reserved */
+    KARA_ECUDA = -5,         /* a CUDA runtime call failed (launch or attribute) */
+    KARA_EBADBLOCK = -6,     /* a block id outside [0, num_blocks) (device) */
+    KARA_ETIMEOUT = -7,      /* a bounded device-side wait ran out (device) */
+    KARA_EWORKSPACE = -8     /* workspace missing or smaller than kara_workspace_size */
+} kara_status;
+
+/* Method parameters.  R is an explicit token count per window. */
+typedef struct {
+    int32_t W;       /* window: the W most recent tokens of a sequence */
+    int32_t B;       /* protected buffer at the end of the window, 0 <= B < W */
+    int32_t K;       /* Top-K candidates per window */
+    int32_t R;       /* tokens each window keeps out of its C compressible ones */
+    float lambda;    /* chunk length penalty in (s_a + s_b) / (1 + lambda * len) */
+} kara_params;
+
+/* Paged K/V pools.  Element (l, blk, g, slot, d) of a pool lives at
+ *   base + l*layer_stride + blk*block_stride + g*head_stride + slot*head_dim + d
+ * (strides in elements).  The canonical layout is
+ * [num_layers][num_blocks][num_kv_heads][block_size][head_dim]. */
+typedef struct {
+    void *k;
+    void *v;
+    int64_t layer_stride, block_stride, head_stride;
+    int32_t num_layers, num_blocks, num_kv_heads, num_q_heads, head_dim, block_size;
+} kara_cache;
+
+/* The sequences compressed by one call. */
+typedef struct {
+    int32_t n;                /* number of sequences */
+    const int32_t *len;       /* device [n]: cached length L of each sequence */
+    int32_t *block_table;     /* device [n][bt_stride]: logical block -> physical id */
+    int32_t bt_stride;
+    const void *q;            /* device bf16 [n][num_layers][num_q_heads][W][head_dim]:
+                                 query states of each sequence's W window tokens */
+} kara_batch;
+
+/* Human-readable name of a status code (static storage). */
+const char *kara_status_string(int status);
+
+/* ABI version of this library. */
+int kara_version(void);
+
+/*
+ * Host-only page plan (summary section 3, "Periodic Compression Policy": the
+ * trailing blocks of selected sequences are compressed and memory is freed).
+ * For each sequence: n_old = ceil(L/bs) - p0 blocks are released and
+ * n_new = ceil(L'/bs) - p0 fresh blocks are taken.  Lets a caller size the
+ * fresh and freed lists before kara_compact / kara_compress_batch.
+ * h_len [n] host; h_n_new, h_n_old [n] host outputs (may be NULL);
+ * h_total_new, h_total_old: sums (may be NULL).
+ * Returns KARA_EINVAL if a length is below W or needs more than bt_stride blocks.
+ */
+kara_status kara_plan(const kara_params *p, int32_t block_size, int32_t n, const int32_t *h_len,
+                      int32_t bt_stride, int32_t *h_n_new, int32_t *h_n_old,
+                      int64_t *h_total_new, int64_t *h_total_old);
+
+/* Bytes of device workspace kara_compact and kara_compress_batch need for n
+ * sequences (256-byte aligned pieces; pass at least this many). */
+size_t kara_workspace_size(const kara_cache *c, const kara_params *p, int32_t n);
+
+/*
+ * Window scores (summary section 1, "Mechanism"/"Rationale"; abstract:
+ * bidirectional attention scores and selects KV pairs).  For every window,
+ * every query head h of the group and every window query i < W:
+ *     p[h,i,j] = softmax_j( <q_{h,i}, k_j> / sqrt(D) ),  j < W  (no causal mask)
+ * and  scores[u][j] = sum_h sum_i p[h,i,j]  for the compressible keys j < C.
+ * k_j is the key at logical position ws + j, read through the block table.
+ * Logits accumulate in fp32 from bf16; the softmax and sums are fp32.
+ * scores: device float [n][num_layers][num_kv_heads][C].
+ * ws/ws_bytes: device workspace; kara_workspace_size bytes always suffice.
+ * err: device int32 (see conventions); a window with a bad block id or a
+ * length below W records the error and writes zeros.
+ */
+kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                       float *scores, void *ws, size_t ws_bytes, int32_t *err,
+                       kara_stream_t stream);
+
+/*
+ * Top-K and Token2Chunk (summary section 1 "Selection"; section 2 "Process").
+ * For each of n_windows windows with C fp32 scores:
+ *   cand: the K positions first in the order (score desc, index asc), sorted
+ *         by index.
+ *   chunks: [c_t, c_{t+1}] for t < K-1, scored
+ *         (s[a] + s[b]) / fmaf(lambda, len, 1), len = b - a + 1, in fp32 with
+ *         round-to-nearest and no contraction; visited by (score desc, a asc)
+ *         and kept when the tokens they add fit R (first fit); then the
+ *         budget is filled to exactly R with candidates, then with other
+ *         positions, both in score order.
+ *   kept: the R retained positions, ascending.
+ * scores [n_windows][C], cand [n_windows][K] (may be NULL), kept [n_windows][R].
+ * Scores must be finite; -0.0 is treated as +0.0.
+ */
+kara_status kara_select(const kara_params *p, int64_t n_windows, const float *scores,
+                        int32_t *cand, int32_t *kept, kara_stream_t stream);
+
+/*
+ * Gather-compaction and block-table rewrite (summary section 3: Kara adapted
+ * to PagedAttention).  For every sequence, layer, KV head and each of K and V,
+ * the new logical positions from p0*bs on are filled with
+ *     [p0*bs, ws)  <- the same old positions (head of the partial block),
+ *     ws + r       <- old ws + kept[u][r], r < R,
+ *     ws + R + b   <- old L - B + b, b < B (protected buffer, verbatim),
+ * written into fresh blocks taken in sequence order from `fresh`.  Only fresh
+ * blocks are written; old blocks are only read.  Then, if *err is still 0, the
+ * table entries [p0, p0 + n_new) become the fresh ids, entries
+ * [p0 + n_new, ceil(L/bs)) become -1, the released ids go to `freed` (in
+ * sequence order) and new_len[s] = L'.  If *err is non-zero nothing is
+ * committed: the table is unchanged, freed is untouched, new_len[s] = L.
+ * kept [n][num_layers][num_kv_heads][R]; fresh [n_fresh] (at least the plan's
+ * total_new); freed [total_old]; new_len [n].
+ * ws/ws_bytes: workspace of kara_workspace_size bytes.
+ */
+kara_status kara_compact(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                         const int32_t *kept, const int32_t *fresh, int64_t n_fresh,
+                         int32_t *freed, int32_t *new_len, int32_t *err,
+                         void *ws, size_t ws_bytes, kara_stream_t stream);
+
+/*
+ * The whole step for a batch: zero *err, plan, score, select, compact and
+ * commit, all on `stream` without a host synchronisation.  scores_out,
+ * cand_out, kept_out may be NULL (then the workspace holds them); when given
+ * they receive [n][layers][Hkv][C], [..][K], [..][R].
+ * phase_events: NULL, or 5 cudaEvent_t handles (cast to void *) that are
+ * recorded on `stream` at the start, after the plan, after scoring, after
+ * selection and after compaction + commit, for callers that time the phases.
+ */
+kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                const int32_t *fresh, int64_t n_fresh, int32_t *freed,
+                                int32_t *new_len, float *scores_out, int32_t *cand_out,
+                                int32_t *kept_out, void *ws, size_t ws_bytes, int32_t *err,
+                                kara_stream_t stream, void *const *phase_events);
+
+/* Waits for `stream`, reads *err and returns it as a status (KARA_ECUDA if the
+ * copy itself fails). */
+kara_status kara_get_error(const int32_t *err, kara_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KARA_H */

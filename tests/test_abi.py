@@ -1,0 +1,113 @@
+"""The C-ABI library loads and exports what include/kara.h declares (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_kv_cache_03_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kara():
+    kbuild.build()
+    from decode_kv_cache_03_gb300 import kara as k
+    return k
+
+
+def declared_functions():
+    names = set()
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(kara_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(kara):
+    lib = ctypes.CDLL(kara.LIB_PATH)
+    names = declared_functions()
+    assert {"kara_score", "kara_select", "kara_compact", "kara_compress_batch", "kara_plan"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kara.EXPORTED) <= names
+
+
+def test_status_strings(kara):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        assert kara.status_string(code).startswith("KARA_")
+    assert kara.version() == 1
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_host_plan_matches_oracle_plan(kara, seed):
+    rng = np.random.default_rng(seed)
+    W = int(rng.choice([64, 128, 512, 1024]))
+    B = int(rng.integers(0, W))
+    R = int(rng.integers(1, W - B + 1))
+    K = 1
+    lengths = rng.integers(W, W + 3000, size=50).astype(np.int32)
+    bt_stride = int((lengths.max() + 15) // 16)
+    nn, no, tn, to = kara.kara_plan(kara.params(W, B, K, R, 0.1), 16, torch.from_numpy(lengths), bt_stride)
+    rn, ro = oracle.plan(lengths, W, B, R, 16, bt_stride)
+    assert nn.numpy().tolist() == rn.tolist() and no.numpy().tolist() == ro.tolist()
+    assert tn == int(rn.sum()) and to == int(ro.sum())
+
+
+def test_host_plan_rejects(kara):
+    p = kara.params(64, 16, 8, 16, 0.1)
+    with pytest.raises(kara.KaraError) as e:
+        kara.kara_plan(p, 16, torch.tensor([63], dtype=torch.int32), 10)
+    assert e.value.status == kara.EINVAL
+    with pytest.raises(kara.KaraError) as e:
+        kara.kara_plan(kara.params(96, 16, 8, 16, 0.1), 16, torch.tensor([200], dtype=torch.int32), 20)
+    assert e.value.status == kara.EUNSUPPORTED
+
+
+def fake_cache(kara, **kw):
+    c = kara.Cache(16, 16, 8 * 16 * 64 * 2, 2 * 16 * 64, 16 * 64, 1, 8, 2, 4, 64, 16)
+    for k_, v_ in kw.items():
+        setattr(c, k_, v_)
+    return c
+
+
+def test_argument_checks_happen_before_any_device_work(kara):
+    """Invalid shapes are refused on the host with a status; nothing is launched."""
+    p = kara.params(64, 16, 8, 16, 0.1)
+    b = kara.Batch(1, 16, 16, 16, 16)
+    ws = ctypes.c_void_p(16)
+    cases = [
+        (fake_cache(kara, head_dim=96), p, kara.EUNSUPPORTED),
+        (fake_cache(kara, block_size=8), p, kara.EUNSUPPORTED),
+        (fake_cache(kara, num_q_heads=3), p, kara.EINVAL),
+        (fake_cache(kara, num_q_heads=2 * 9), p, kara.EUNSUPPORTED),
+        (fake_cache(kara, k=None), p, kara.EINVAL),
+        (fake_cache(kara, k=18), p, kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 64, 8, 16, 0.1), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 49, 16, 0.1), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 8, 49, 0.1), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 8, 0, 0.1), kara.EINVAL),
+        (fake_cache(kara), kara.params(4096, 16, 8, 16, 0.1), kara.EUNSUPPORTED),
+    ]
+    for c, pp, want in cases:
+        st = kara._lib.kara_compress_batch(ctypes.byref(c), ctypes.byref(pp), ctypes.byref(b), ws, 4, ws, ws,
+                                           None, None, None, ws, 1 << 30, ws, None, None)
+        assert st == want, (c.head_dim, pp.W, st)
+    # workspace too small is refused before launching
+    st = kara._lib.kara_compress_batch(ctypes.byref(fake_cache(kara)), ctypes.byref(p), ctypes.byref(b), ws, 4,
+                                       ws, ws, None, None, None, ws, 1, ws, None, None)
+    assert st == kara.EWORKSPACE
+
+
+def test_workspace_size_grows_with_batch(kara):
+    c = fake_cache(kara)
+    p = kara.params(64, 16, 8, 16, 0.1)
+    a, b = kara.kara_workspace_size(c, p, 1), kara.kara_workspace_size(c, p, 10)
+    assert 0 < a < b
+    assert kara.kara_workspace_size(fake_cache(kara, head_dim=96), p, 1) == 0

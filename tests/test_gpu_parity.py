@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _cases import random_spec
+from _gpu import SCORE_RTOL, lib, rel_err, run_compress, stable_windows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, **kw):
+    return synth.SPECS[name].with_(**kw)
+
+
+E2E_CASES = {
+    "tiny": synth.SPECS["tiny"],
+    "qwen3_4b_small": small("qwen3_4b", n_seq=3, layers=2),
+    "qwen3_14b_small": small("qwen3_14b", n_seq=2, layers=1, len_lo=2048, len_hi=4100),
+    "llama_8b_small": small("llama_8b", n_seq=4, layers=2, len_lo=1024, len_hi=2100),
+    "sweep_w128": synth.sweep_spec(4, 128).with_(layers=2),
+    "sweep_w2048": synth.sweep_spec(1, 2048).with_(layers=1),
+    "ragged_g3": random_spec(77, G=3, hkv=2, W=192, B=40, D=128, n_seq=3, layers=2, K=20, R=50,
+                             len_lo=192, len_hi=400),
+}
+
+
+@pytest.mark.parametrize("case", list(E2E_CASES))
+def test_compress_batch_matches_oracle(case):
+    spec = E2E_CASES[case]
+    wl = synth.generate(spec)
+    out = run_compress(to_device(wl))
+    assert out["status"] == 0
+    sh = oracle.shape_of(wl)
+    ref = oracle.scores(sh, wl.q, wl.k, wl.block_table, wl.lengths)
+    # 1. scores within 1e-3 relative, element by element
+    err = rel_err(out["scores"], ref)
+    assert err.max() <= SCORE_RTOL, f"max rel err {err.max():.3e}"
+    # 2. selection on the GPU's own scores is bit-exact
+    cand_o, kept_o = oracle.select_batch(out["scores"], spec.K, spec.R, spec.lam)
+    assert np.array_equal(out["cand"], cand_o)
+    assert np.array_equal(out["kept"], kept_o)
+    # 3. compaction, tables, freed ids and lengths bit-exact given the GPU's kept
+    st, k2, v2, bt2, freed, new_len = oracle.compact(sh, wl.k, wl.v, wl.block_table, wl.lengths,
+                                                     out["kept"], wl.fresh)
+    assert st == oracle.OK
+    assert np.array_equal(out["bt"], bt2)
+    assert np.array_equal(out["freed"], freed)
+    assert np.array_equal(out["new_len"], new_len)
+    assert np.array_equal(out["k"], k2) and np.array_equal(out["v"], v2)
+    # 4. end to end against the oracle's own selection, on tolerance-stable windows
+    _, kept_ref = oracle.select_batch(ref, spec.K, spec.R, spec.lam)
+    same = np.all(out["kept"] == kept_ref, axis=-1)
+    stable = stable_windows(ref, spec.K, spec.R, spec.lam)
+    assert np.all(same[stable]), f"{(~same[stable]).sum()} stable windows differ"
+    assert same.mean() >= 0.9, f"exact-match rate {same.mean():.3f}"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_select_bitexact_with_ties(seed):
+    kara = lib()
+    rng = np.random.default_rng(seed)
+    W = int(rng.choice([64, 512, 1024, 2048]))
+    B = int(rng.choice([0, 16, W // 8]))
+    C = W - B
+    K = int(rng.choice([1, 2, 8, min(C, 256), min(C, 1024)]))
+    R = int(rng.choice([1, K, min(C, 89), C // 2, C]))
+    nwin = 37
+    if seed % 2:
+        s = rng.choice(np.float32([0.5, 1.0, 1.0000001, 2.0, 0.0, -0.0]), size=(nwin, C))
+    else:
+        s = rng.exponential(size=(nwin, C)).astype(np.float32)
+    sc = torch.from_numpy(s.astype(np.float32)).cuda()
+    cand = torch.empty(nwin, K, dtype=torch.int32, device="cuda")
+    kept = torch.empty(nwin, R, dtype=torch.int32, device="cuda")
+    kara.kara_select(kara.params(W, B, K, R, 0.1), nwin, sc, cand, kept)
+    torch.cuda.synchronize()
+    c_o, k_o = oracle.select_batch(s, K, R, 0.1)
+    assert np.array_equal(cand.cpu().numpy(), c_o)
+    assert np.array_equal(kept.cpu().numpy(), k_o)
+
+
+def test_score_alone_matches_oracle():
+    kara = lib()
+    spec = random_spec(5, G=4, hkv=2, W=256, B=32, D=128, n_seq=2, layers=2, len_lo=300, len_hi=700)
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    c = kara.cache(d.k, d.v, spec.hq)
+    p = kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam)
+    b = kara.batch(d.lengths, d.block_table, d.q)
+    scores = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.C, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_score(c, p, b, scores, ws, err)
+    assert kara.kara_get_error(err) == 0
+    ref = oracle.scores(oracle.shape_of(wl), wl.q, wl.k, wl.block_table, wl.lengths)
+    assert rel_err(scores.cpu().numpy(), ref).max() <= SCORE_RTOL
+
+
+def test_compact_alone_with_oracle_kept():
+    kara = lib()
+    spec = random_spec(6, G=2, hkv=2, W=128, B=16, D=64, n_seq=3, layers=2, R=30, len_lo=128, len_hi=300)
+    wl = synth.generate(spec)
+    rng = np.random.default_rng(1)
+    kept = np.sort(np.stack([rng.choice(spec.C, spec.R, replace=False)
+                             for _ in range(spec.n_windows)]), axis=-1).astype(np.int32)
+    kept = kept.reshape(spec.n_seq, spec.layers, spec.hkv, spec.R)
+    d = to_device(wl)
+    c = kara.cache(d.k, d.v, spec.hq)
+    p = kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam)
+    bt = d.block_table.clone()
+    b = kara.batch(d.lengths, bt, d.q)
+    _, _, tn, to = kara.kara_plan(p, 16, wl.lengths, wl.bt_stride)
+    freed = torch.empty(to, dtype=torch.int32, device="cuda")
+    new_len = torch.empty(spec.n_seq, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_compact(c, p, b, torch.from_numpy(kept).cuda(), d.fresh, freed, new_len, err, ws)
+    assert kara.kara_get_error(err) == 0
+    st, k2, v2, bt2, fr2, nl2 = oracle.compact(oracle.shape_of(wl), wl.k, wl.v, wl.block_table, wl.lengths,
+                                              kept, wl.fresh)
+    assert np.array_equal(bt.cpu().numpy(), bt2) and np.array_equal(freed.cpu().numpy(), fr2)
+    assert np.array_equal(new_len.cpu().numpy(), nl2)
+    assert np.array_equal(d.k.view(torch.int16).cpu().numpy().view(np.uint16), k2)
+    assert np.array_equal(d.v.view(torch.int16).cpu().numpy().view(np.uint16), v2)
+
+
+def _error_case(mutate):
+    spec = random_spec(8, G=2, hkv=2, W=64, B=16, D=64, n_seq=3, layers=1, R=16)
+    wl = synth.generate(spec)
+    n_fresh = mutate(wl)
+    d = to_device(wl)
+    k0, v0, bt0 = d.k.clone(), d.v.clone(), d.block_table.clone()
+    out = run_compress(d, n_fresh=n_fresh)
+    return wl, out, k0, v0, bt0
+
+
+def _assert_nothing_committed(wl, out, bt0):
+    assert np.array_equal(out["bt"], bt0.cpu().numpy())
+    assert np.array_equal(out["new_len"], wl.lengths.numpy())
+    # old (non-fresh) blocks are never written
+    fb = wl.fresh_base
+    assert np.array_equal(out["k"][:, :fb], wl.k.view(torch.int16).numpy().view(np.uint16)[:, :fb])
+
+
+def test_bad_block_id_is_reported_and_nothing_committed():
+    def mutate(wl):
+        L = int(wl.lengths[1])
+        wl.block_table[1, (L - 1) // 16] = wl.num_blocks + 3
+    wl, out, _, _, bt0 = _error_case(mutate)
+    assert out["status"] == lib().EBADBLOCK
+    _assert_nothing_committed(wl, out, bt0)
+
+
+def test_short_fresh_list_is_reported_and_nothing_committed():
+    wl, out, _, _, bt0 = _error_case(lambda wl: 1)
+    assert out["status"] == lib().ENOBLOCKS
+    _assert_nothing_committed(wl, out, bt0)
+
+
+def test_short_sequence_is_reported_and_nothing_committed():
+    def mutate(wl):
+        wl.lengths[2] = 40
+    spec = random_spec(8, G=2, hkv=2, W=64, B=16, D=64, n_seq=3, layers=1, R=16)
+    wl = synth.generate(spec)
+    mutate(wl)
+    d = to_device(wl)
+    kara = lib()
+    # the host plan refuses it too
+    with pytest.raises(kara.KaraError):
+        kara.kara_plan(kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam), 16, wl.lengths, wl.bt_stride)
+    bt0 = d.block_table.clone()
+    s = spec
+    c = kara.cache(d.k, d.v, s.hq)
+    p = kara.params(s.W, s.B, s.K, s.R, s.lam)
+    bt = d.block_table.clone()
+    b = kara.batch(d.lengths, bt, d.q)
+    freed = torch.full((64,), -7, dtype=torch.int32, device="cuda")
+    new_len = torch.empty(s.n_seq, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kara.kara_workspace_size(c, p, s.n_seq), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_compress_batch(c, p, b, d.fresh, freed, new_len, ws, err)
+    assert kara.kara_get_error(err) == kara.EINVAL
+    assert torch.equal(bt, bt0)
+    assert torch.equal(new_len.cpu(), wl.lengths)
+    assert torch.all(freed == -7)
