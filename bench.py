@@ -231,6 +231,10 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for row in ev:                         # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
 
     def step(events=None):
         bt.copy_(bt0)                      # every step compresses the same trailing windows

@@ -1,53 +1,35 @@
 """Kara decode-time KV-cache compression on GB300 (sm_103a).
 
 The work runs in ``libkara.so`` (hand-written CUDA, C ABI in include/kara.h);
-``decode_kv_cache_03_gb300.kara`` is its ctypes binding.  ``Compressor`` is a
-convenience wrapper that owns the workspace and error word for one cache.
+``decode_kv_cache_03_gb300.kara`` is its ctypes binding and raises on import if
+the library is missing.  ``decode_kv_cache_03_gb300.build`` compiles it.
+``Compressor`` wraps the workspace and error word for one cache.  Names are
+resolved lazily so that the build module can be imported before the library
+exists.
 """
 from __future__ import annotations
 
-import torch
+import importlib
 
-from . import kara
-from .kara import KaraError, kara_compact, kara_compress_batch, kara_get_error, kara_plan, kara_score, \
-    kara_select, kara_workspace_size
+_LAZY = {
+    "kara": ("kara", None),
+    "Compressor": ("compressor", "Compressor"),
+    "KaraError": ("kara", "KaraError"),
+    "kara_plan": ("kara", "kara_plan"),
+    "kara_workspace_size": ("kara", "kara_workspace_size"),
+    "kara_score": ("kara", "kara_score"),
+    "kara_select": ("kara", "kara_select"),
+    "kara_compact": ("kara", "kara_compact"),
+    "kara_compress_batch": ("kara", "kara_compress_batch"),
+    "kara_get_error": ("kara", "kara_get_error"),
+}
 
-
-class Compressor:
-    """Periodic compression of the trailing windows of selected sequences.
-
-    Holds the device workspace and error word; the cache, tables and fresh
-    block ids stay owned by the caller.
-    """
-
-    def __init__(self, k: torch.Tensor, v: torch.Tensor, num_q_heads: int, W: int, B: int, K: int, R: int,
-                 lam: float = 0.1):
-        self.k, self.v = k, v
-        self.cache = kara.cache(k, v, num_q_heads)
-        self.params = kara.params(W, B, K, R, lam)
-        self.err = torch.zeros(1, dtype=torch.int32, device=k.device)
-        self._ws = torch.empty(0, dtype=torch.uint8, device=k.device)
-
-    def workspace(self, n: int) -> torch.Tensor:
-        need = kara_workspace_size(self.cache, self.params, n)
-        if self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=self.k.device)
-        return self._ws
-
-    def plan(self, lengths_host: torch.Tensor, bt_stride: int):
-        return kara_plan(self.params, self.cache.block_size, lengths_host, bt_stride)
-
-    def compress(self, lengths, block_table, q, fresh, freed, new_len, scores=None, cand=None, kept=None,
-                 stream=None):
-        """Enqueue the whole step; block_table is rewritten in place on success."""
-        b = kara.batch(lengths, block_table, q)
-        ws = self.workspace(b.n)
-        kara_compress_batch(self.cache, self.params, b, fresh, freed, new_len, ws, self.err, scores, cand,
-                            kept, stream)
-
-    def error(self, stream=None) -> int:
-        return kara_get_error(self.err, stream)
+__all__ = sorted(_LAZY)
 
 
-__all__ = ["Compressor", "KaraError", "kara", "kara_compact", "kara_compress_batch", "kara_get_error",
-           "kara_plan", "kara_score", "kara_select", "kara_workspace_size"]
+def __getattr__(name):
+    if name not in _LAZY:
+        raise AttributeError(name)
+    mod, attr = _LAZY[name]
+    m = importlib.import_module(f".{mod}", __name__)
+    return m if attr is None else getattr(m, attr)

@@ -156,7 +156,8 @@ def kara_compress_batch(c: Cache, p: Params, b: Batch, fresh, freed, new_len, ws
     ev = None
     if phase_events is not None:
         assert len(phase_events) == 5
-        ev = (ctypes.c_void_p * 5)(*[e.cuda_event for e in phase_events])
+        assert all(e.cuda_event for e in phase_events), "record each event once before passing it"
+        ev =(ctypes.c_void_p * 5)(*[e.cuda_event for e in phase_events])
     _check(_lib.kara_compress_batch(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(fresh),
                                     int(fresh.numel()), _ptr(freed), _ptr(new_len), _ptr(scores_out),
                                     _ptr(cand_out), _ptr(kept_out), _ptr(ws), ws.numel() * ws.element_size(),
