@@ -58,6 +58,9 @@ __device__ __forceinline__ int64_t pool_off(const Geo &g, int l, int32_t blk, in
 
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Host-side argument checks of the entry points; fills the geometry of a call.
+kara_status geo_from_args(const kara_cache *c, const kara_params *p, const kara_batch *b, Geo *g);
+
 // Launchers (each returns the launch error, if any).
 cudaError_t launch_plan(const Geo &g, int64_t n_fresh, SeqPlan *plan, int32_t *err, cudaStream_t st);
 cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,

@@ -109,6 +109,14 @@ kara_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KARA_OK : KAR
 
 }  // namespace
 
+namespace kara {
+// The argument checks and geometry of the entry points, for other sources of the library.
+kara_status geo_from_args(const kara_cache *c, const kara_params *p, const kara_batch *b, Geo *g)
+{
+    return make_geo(c, p, b, g);
+}
+}  // namespace kara
+
 extern "C" {
 
 const char *kara_status_string(int status)

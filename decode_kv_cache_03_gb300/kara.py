@@ -61,6 +61,7 @@ def _load():
         "kara_compact": ([PC, PP, PB, P, P, I64, P, P, P, P, SZ, P], ctypes.c_int),
         "kara_compress_batch": ([PC, PP, PB, P, I64, P, P, P, P, P, P, SZ, P, P, P], ctypes.c_int),
         "kara_get_error": ([P, P], ctypes.c_int),
+        "kara_compact_static": ([PC, PP, PB, P, P, I64, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -71,7 +72,8 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("kara_status_string", "kara_version", "kara_plan", "kara_workspace_size", "kara_score",
-            "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error")
+            "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error", "kara_compact_static")
+STATIC_MAX_SEQS = 8192     # KARA_STATIC_MAX_SEQS
 
 
 def status_string(status: int) -> str:
@@ -150,6 +152,13 @@ def kara_compact(c: Cache, p: Params, b: Batch, kept, fresh, freed, new_len, err
                              ws.numel() * ws.element_size(), _stream(stream)), "kara_compact")
 
 
+def kara_compact_static(c: Cache, p: Params, b: Batch, kept, fresh, freed, new_len, err, stream=None):
+    """kara_compact without a workspace (plan kept in the library's fixed array)."""
+    _check(_lib.kara_compact_static(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(kept), _ptr(fresh),
+                                    int(fresh.numel()), _ptr(freed), _ptr(new_len), _ptr(err), _stream(stream)),
+           "kara_compact_static")
+
+
 def kara_compress_batch(c: Cache, p: Params, b: Batch, fresh, freed, new_len, ws, err, scores_out=None,
                         cand_out=None, kept_out=None, stream=None, phase_events=None):
     """phase_events: None or 5 torch.cuda.Event(enable_timing=True) recorded around the phases."""
@@ -157,7 +166,7 @@ def kara_compress_batch(c: Cache, p: Params, b: Batch, fresh, freed, new_len, ws
     if phase_events is not None:
         assert len(phase_events) == 5
         assert all(e.cuda_event for e in phase_events), "record each event once before passing it"
-        ev =(ctypes.c_void_p * 5)(*[e.cuda_event for e in phase_events])
+        ev = (ctypes.c_void_p * 5)(*[e.cuda_event for e in phase_events])
     _check(_lib.kara_compress_batch(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(fresh),
                                     int(fresh.numel()), _ptr(freed), _ptr(new_len), _ptr(scores_out),
                                     _ptr(cand_out), _ptr(kept_out), _ptr(ws), ws.numel() * ws.element_size(),

@@ -190,6 +190,38 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
  * copy itself fails). */
 kara_status kara_get_error(const int32_t *err, kara_stream_t stream);
 
+/* Most sequences one kara_compact_static call accepts. */
+#define KARA_STATIC_MAX_SEQS 8192
+
+/*
+ * kara_compact_static -- kara_compact without a workspace.  The paper has no
+ * counterpart; this is a deployment convenience.
+ *
+ * For callers that cannot get device memory when compaction runs: a serving
+ * engine whose memory pool handed all free HBM to the KV cache at start-up,
+ * or a host program that embeds this library without any device allocator.
+ * Such a caller passes its inputs and outputs exactly as for kara_compact
+ * (same meaning, layout, ownership and commit rule) but no workspace; the
+ * per-sequence plan lives in a fixed array inside the library instead:
+ * KARA_STATIC_MAX_SEQS entries of 32 bytes (256 KiB), held by every GPU that
+ * loads the library until the process exits.
+ *   - More than KARA_STATIC_MAX_SEQS sequences: returns KARA_EUNSUPPORTED
+ *     before any device work.  Split the batch.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call uses the same array and it keeps the last call's contents.
+ *     Nothing has to be cleared between calls (each call writes every entry
+ *     it reads), but calls whose work overlaps on the GPU -- two streams with
+ *     no ordering between them, or two host threads -- race on the array and
+ *     corrupt each other's plan.  Calls ordered on one stream are safe.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.
+ */
+kara_status kara_compact_static(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                const int32_t *kept, const int32_t *fresh, int64_t n_fresh,
+                                int32_t *freed, int32_t *new_len, int32_t *err,
+                                kara_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
