@@ -200,6 +200,10 @@ def main():
     ap.add_argument("--config", default="qwen3_14b", choices=sorted(synth.SPECS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--n-seq", type=int, default=None, help="override the workload's sequence count")
+    ap.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
+    ap.add_argument("--profile-kernel", choices=["score", "select", "compact"], default=None,
+                    help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
     args = ap.parse_args()
     ws_, rank, local = dist_setup()
     if args.impl == "reference":
@@ -215,6 +219,10 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     spec = synth.SPECS[args.config].with_(seed=synth.SPECS[args.config].seed + 97 * rank)
+    if args.n_seq:
+        spec = spec.with_(n_seq=args.n_seq)
+    if args.layers:
+        spec = spec.with_(layers=args.layers)
     wl = synth.generate(spec, device=dev)
     torch.cuda.synchronize()
     c = kara.cache(wl.k, wl.v, spec.hq)
@@ -235,6 +243,10 @@ def main():
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+
+    if args.profile_kernel:
+        profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err)
+        return
 
     def step(events=None):
         bt.copy_(bt0)                      # every step compresses the same trailing windows
@@ -352,8 +364,32 @@ def main():
 
 
 def launches_per_step():
-    """Kernels of this library per kara_compress_batch: plan, score (2), select, compact, commit."""
-    return 6
+    """Kernels of this library per kara_compress_batch: plan, score, select, compact, commit."""
+    return 5
+
+
+def profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err):
+    """Runs one entry point on the resident workload `--steps` times (ncu target)."""
+    nwin = spec.n_windows
+    scores = torch.empty(nwin, spec.C, dtype=torch.float32, device=wl.q.device)
+    kept = torch.empty(nwin, spec.R, dtype=torch.int32, device=wl.q.device)
+    kara.kara_score(c, p, b, scores, ws, err)
+    kara.kara_select(p, nwin, scores, None, kept)
+    torch.cuda.synchronize()
+    bt0 = wl.block_table.clone()
+    for _ in range(args.steps):
+        if args.profile_kernel == "score":
+            kara.kara_score(c, p, b, scores, ws, err)
+        elif args.profile_kernel == "select":
+            kara.kara_select(p, nwin, scores, None, kept)
+        else:
+            wl.block_table.copy_(bt0)
+            kara.kara_compact(c, p, b, kept, fresh, freed, new_len, err, ws)
+    torch.cuda.synchronize()
+    status = kara.kara_get_error(err)
+    if status != 0:
+        raise SystemExit(f"{args.profile_kernel} reported {kara.status_string(status)}")
+    print(f"profiled {args.profile_kernel} x{args.steps} on {nwin} windows", flush=True)
 
 
 if __name__ == "__main__":

@@ -11,6 +11,7 @@ namespace {
 
 constexpr int kMaxK = 1024;
 constexpr int kMaxG = 8;
+constexpr int kMaxGW = 8192;  // query rows per window the scoring kernel keeps statistics for
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -51,6 +52,7 @@ kara_status make_geo(const kara_cache *c, const kara_params *p, const kara_batch
     if (!b || b->n < 0) return KARA_EINVAL;
     if (b->n > 0 && (!b->len || !b->block_table || !b->q || b->bt_stride < 1)) return KARA_EINVAL;
     if (b->q && !aligned16(b->q)) return KARA_EINVAL;
+    if ((c->num_q_heads / c->num_kv_heads) * p->W > kMaxGW) return KARA_EUNSUPPORTED;
     memset(g, 0, sizeof *g);
     g->k = static_cast<const uint16_t *>(c->k);
     g->v = static_cast<const uint16_t *>(c->v);
@@ -164,6 +166,7 @@ kara_status kara_plan(const kara_params *p, int32_t block_size, int32_t n, const
 size_t kara_workspace_size(const kara_cache *c, const kara_params *p, int32_t n)
 {
     if (check_params(p) != KARA_OK || check_cache(c) != KARA_OK || n < 0) return 0;
+    if ((c->num_q_heads / c->num_kv_heads) * p->W > kMaxGW) return 0;
     Geo g;
     memset(&g, 0, sizeof g);
     g.layers = c->num_layers;

@@ -1,0 +1,478 @@
+// Window scoring on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Follows the gist.science summary of Kara (arXiv 2607.01237), section
+// "1. Sliding-Window Bidirectional Attention Scoring" (Mechanism, Rationale):
+// the query states of all W window tokens score the keys of the window with
+// bidirectional attention (no causal mask) and the attention weights are
+// accumulated.  For window u = (sequence, layer, KV head g):
+//     p[h,i,j] = softmax_j( <q_{h,i}, k_j> / sqrt(D) ),  i, j < W, h in group g
+//     s[j]     = sum_h sum_i p[h,i,j],  j < C = W - B
+// The softmax of a query row runs over all W window keys; keys j >= C (the
+// protected buffer) take part in the normalisation but are not scored.
+//
+// Work decomposition: one thread-block cluster per window, one CTA per slice of
+// up to 256 window keys (cluster size ceil(W/256) <= 8).  Each CTA gathers its
+// key slice once through the block table into shared memory (128-byte
+// swizzled, the layout the tensor core reads) and streams the window's query
+// rows through a TMA ring of 128-row strips, twice:
+//
+//   pass 1  S = Q_strip * K_slice^T  (M = 128 query rows, N = slice) into TMEM;
+//           per row the slice's max and sum of exponentials (fp32);
+//           the cluster then merges the slices' (max, sum) pairs through
+//           distributed shared memory into lse2[row] = log2 sum_j 2^(l2_j),
+//           l2 = <q,k> * log2(e)/sqrt(D).
+//   pass 2  S^T = K_tile * Q_strip^T (M = 128 keys of the slice's compressible
+//           part, N = 128 query rows): key rows sit on TMEM lanes, so each
+//           thread owns one key and sums 2^(l2 - lse2[row]) over its row of
+//           TMEM -- the column sum needs no cross-thread reduction.
+//
+// No W x W matrix ever reaches memory; every score is a deterministic fp32 sum.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 allocates TMEM and
+// issues MMAs (one elected lane), warps 2..9 read TMEM (softmax / sums).  Every
+// wait on an mbarrier is bounded; on time-out the CTA records KARA_ETIMEOUT,
+// stops issuing work, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "kara_common.cuh"
+#include "kara_sm100.cuh"
+
+namespace kara {
+namespace {
+
+using namespace ptx;
+
+constexpr int kSlice = 256;        // keys per CTA
+constexpr int kStrip = 128;        // query rows per strip
+constexpr int kThreads = 320;
+constexpr int kSoftThreads = 256;  // warps 2..9
+constexpr int kMaxStages = 4;
+constexpr int kMaxRowsPerThread = 32;  // (G*W rounded up to 128) / 256, G*W <= 8192
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s: every wait here normally ends in microseconds
+
+template <int D>
+struct Cfg {
+    static constexpr int kAtoms = D / 64;              // 128-byte swizzle atoms per row
+    static constexpr int kKBytes = kSlice * D * 2;
+    static constexpr int kQBytes = kStrip * D * 2;
+    static constexpr int kKAtomBytes = kSlice * 128;   // one atom of the key slice
+    static constexpr int kQAtomBytes = kStrip * 128;   // one atom of a query strip
+    static constexpr int kKSteps = D / 16;
+};
+
+struct Shared {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    int bad;
+};
+
+// Dynamic shared memory of one CTA.  Never below 120 KB: with more than half
+// of the SM's shared memory no second CTA can share the SM, so a CTA never
+// waits in tcgen05.alloc for TMEM that a cluster peer on the same SM holds
+// while that peer waits for it at a cluster barrier.
+constexpr size_t kMinSmem = 120 * 1024;
+
+size_t smem_bytes(int D, int T, int stages)
+{
+    const size_t kb = (size_t)kSlice * D * 2, qb = (size_t)kStrip * D * 2;
+    const size_t need = 1024 + kb + stages * qb + (size_t)T * kStrip * 8 + 2 * kStrip * 8 + sizeof(Shared);
+    return need > kMinSmem ? need : kMinSmem;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (without waiting) once the
+// CTA has aborted, or after recording a time-out.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *err, bool honour_abort = true)
+{
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (honour_abort && *(volatile int *)&sh->abort) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kTimeoutNs) {
+                set_err(err, KARA_ETIMEOUT);
+                *(volatile int *)&sh->abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
+                    int32_t *err, int ncta, int T, int stages, float c2)
+{
+    using C_ = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t *sK = base;
+    uint8_t *sQ = sK + C_::kKBytes;
+    float2 *part = reinterpret_cast<float2 *>(sQ + stages * C_::kQBytes);
+    float2 *xbuf = part + T * kStrip;                       // [2][128]
+    Shared *sh = reinterpret_cast<Shared *>(xbuf + 2 * kStrip);
+    const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+    const int64_t u = blockIdx.x / ncta;
+    int s, l, h;
+    window_coords(g, u, s, l, h);
+    const int GW = g.G * g.W;
+    const int slice0 = (int)crank * kSlice;
+    const int S = min(kSlice, g.W - slice0);                // keys of this CTA (multiple of 64)
+    const int Cc = max(0, min(S, g.C - slice0));            // compressible keys of this CTA
+    const int nM = (Cc + 127) / 128;                        // pass-2 M tiles (0..2)
+    const int T2 = nM > 0 ? T : 0;
+
+    // -- validity of the window (uniform over the cluster) --------------------
+    const int32_t L = g.len[s];
+    bool valid = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
+    if (threadIdx.x == 0) { sh->abort = 0; sh->bad = 0; }
+    __syncthreads();
+    const int32_t ws = L - g.W;
+    const int32_t *btr = g.bt + (int64_t)s * g.bt_stride;
+    if (valid) {
+        const int nb = (L + g.bs - 1) / g.bs - ws / g.bs;
+        for (int t = threadIdx.x; t < nb; t += kThreads) {
+            const int32_t b = btr[ws / g.bs + t];
+            if (b < 0 || b >= g.num_blocks) sh->bad = 1;
+        }
+    }
+    __syncthreads();
+    if (!valid || sh->bad) {
+        if (threadIdx.x == 0) set_err(err, valid ? KARA_EBADBLOCK : KARA_EINVAL);
+        for (int j = threadIdx.x; j < Cc; j += kThreads) scores[u * g.C + slice0 + j] = 0.f;
+        return;
+    }
+
+    // -- set-up: barriers, TMEM, key slice -------------------------------------
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(smem_u32(&sh->full[i]), 1);
+            mbar_init(smem_u32(&sh->empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sh->tfull[i]), 1);
+            mbar_init(smem_u32(&sh->tempty[i]), kSoftThreads / 32);
+        }
+        mbar_init(smem_u32(&sh->done), 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmap);
+    // Key rows slice0 .. slice0+S-1 of the window, 16 bytes per copy, written in
+    // the 128-byte swizzled K-major layout: chunk c of row r of atom a lands at
+    // atom_base + r*128 + ((c ^ (r & 7)) * 16).
+    {
+        constexpr int CPR = D / 8;  // 16-byte chunks per row
+        for (int idx = threadIdx.x; idx < S * CPR; idx += kThreads) {
+            const int r = idx / CPR, cc = idx % CPR;
+            const int x = ws + slice0 + r;
+            const int32_t blk = btr[x / g.bs];
+            const uint16_t *src = g.k + pool_off(g, l, blk, h, x % g.bs) + cc * 8;
+            const int a = cc >> 3, c8 = cc & 7;
+            const uint32_t dst = sK_u + a * C_::kKAtomBytes + r * 128 + ((c8 ^ (r & 7)) << 4);
+            cp_async16(dst, src);
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- producer: query strips by TMA ----------------------
+        const int row0 = ((s * g.layers + l) * g.hq + h * g.G) * g.W;
+        const int pre = min(stages, T2);
+        int issued = 0;
+        auto produce = [&](int j) {
+            const int st = j % stages;
+            if (!wait_phase(smem_u32(&sh->empty[st]), ((j / stages) & 1) ^ 1, sh, err)) return;
+            const uint32_t fb = smem_u32(&sh->full[st]);
+            mbar_arrive_expect_tx(fb, C_::kQBytes);
+            const int t = j < T ? j : j - T;
+#pragma unroll
+            for (int a = 0; a < C_::kAtoms; ++a)
+                tma_load_2d(sQ_u + st * C_::kQBytes + a * C_::kQAtomBytes, &tmap, fb, a * 64, row0 + t * kStrip);
+            issued = j + 1;
+        };
+        if (lane == 0)
+            for (int j = 0; j < T + pre; ++j) produce(j);
+        __syncwarp();
+        cluster_arrive();
+        cluster_wait();
+        cluster_arrive();
+        if (lane == 0) {
+            for (int j = T + pre; j < T + T2; ++j) produce(j);
+            // drain: every issued copy has landed before this CTA may exit
+            for (int j = max(0, issued - stages); j < issued; ++j)
+                wait_phase(smem_u32(&sh->full[j % stages]), (j / stages) & 1, sh, err, false);
+        }
+        __syncwarp();
+        cluster_wait();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer -----------------------------------------
+        const uint32_t idesc1 = idesc_bf16(128, S);
+        const uint32_t idesc2 = idesc_bf16(128, 128);
+        if (lane == 0) {
+            for (int t = 0; t < T; ++t) {
+                const int st = t % stages, b = t & 1;
+                if (!wait_phase(smem_u32(&sh->full[st]), (t / stages) & 1, sh, err)) break;
+                if (!wait_phase(smem_u32(&sh->tempty[b]), ((t >> 1) & 1) ^ 1, sh, err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C_::kKSteps; ++kk) {
+                    const int a = kk >> 2, off = (kk & 3) * 32;
+                    const uint64_t ad = sdesc_sw128(sQ_u + st * C_::kQBytes + a * C_::kQAtomBytes + off);
+                    const uint64_t bd = sdesc_sw128(sK_u + a * C_::kKAtomBytes + off);
+                    mma_bf16(tmem + b * 256, ad, bd, idesc1, kk > 0);
+                }
+                mma_commit(smem_u32(&sh->empty[st]));
+                mma_commit(smem_u32(&sh->tfull[b]));
+            }
+        }
+        __syncwarp();
+        cluster_arrive();
+        cluster_wait();
+        cluster_arrive();
+        if (lane == 0) {
+            for (int t = 0; t < T2; ++t) {
+                const int j = T + t, st = j % stages, b = j & 1;
+                if (!wait_phase(smem_u32(&sh->full[st]), (j / stages) & 1, sh, err)) break;
+                if (!wait_phase(smem_u32(&sh->tempty[b]), ((j >> 1) & 1) ^ 1, sh, err)) break;
+                tc_fence_after();
+                for (int mt = 0; mt < nM; ++mt) {
+#pragma unroll
+                    for (int kk = 0; kk < C_::kKSteps; ++kk) {
+                        const int a = kk >> 2, off = (kk & 3) * 32;
+                        const uint64_t ad = sdesc_sw128(sK_u + a * C_::kKAtomBytes + mt * (128 * 128) + off);
+                        const uint64_t bd = sdesc_sw128(sQ_u + st * C_::kQBytes + a * C_::kQAtomBytes + off);
+                        mma_bf16(tmem + b * 256 + mt * 128, ad, bd, idesc2, kk > 0);
+                    }
+                }
+                mma_commit(smem_u32(&sh->empty[st]));
+                mma_commit(smem_u32(&sh->tfull[b]));
+            }
+            // every MMA issued has completed before TMEM is freed
+            mma_commit(smem_u32(&sh->done));
+            wait_phase(smem_u32(&sh->done), 0, sh, err, false);
+        }
+        __syncwarp();
+        cluster_wait();
+    } else {
+        // ---------------- softmax / column sums (warps 2..9) -------------------
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int row = 32 * q4 + lane;
+        const int sidx = (warp - 2) * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const int half = S >> 1, nld = half >> 5;  // 1..4 loads of 32 columns
+
+        // pass 1: row max and sum of exponentials over this CTA's keys
+        for (int t = 0; t < T; ++t) {
+            const int b = t & 1;
+            wait_phase(smem_u32(&sh->tfull[b]), (t >> 1) & 1, sh, err);
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t ta = tmem + lane_base + b * 256 + hf * half;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < nld) tmem_ld32(ta + k * 32, v[k]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < nld) tmem_wait_ld(v[k]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+            float m = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < nld)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) m = fmaxf(m, __uint_as_float(v[k][i]));
+            const float mc = m * c2;
+            float z = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < nld)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z += ex2(fmaf(__uint_as_float(v[k][i]), c2, -mc));
+            if (hf == 1) xbuf[b * kStrip + row] = make_float2(mc, z);
+            named_barrier(1, kSoftThreads);
+            if (hf == 0) {
+                const float2 o = xbuf[b * kStrip + row];
+                const float M = fmaxf(mc, o.x);
+                const float Z = z * ex2(mc - M) + o.y * ex2(o.x - M);
+                const int r = t * kStrip + row;
+                if (r < GW) part[r] = make_float2(M, Z);
+            }
+        }
+        __syncwarp();
+        cluster_arrive();
+        cluster_wait();
+        // merge the slices' (max, sum) of every query row across the cluster
+        const int TT = T * kStrip;
+        float lse[kMaxRowsPerThread];
+#pragma unroll
+        for (int k = 0; k < kMaxRowsPerThread; ++k) {
+            const int r = sidx + k * kSoftThreads;
+            lse[k] = INFINITY;
+            if (r < GW) {
+                float2 pr[8];
+                float M = -INFINITY;
+                const uint32_t la = smem_u32(&part[r]);
+#pragma unroll
+                for (int cr = 0; cr < 8; ++cr) {
+                    if (cr < ncta) {
+                        pr[cr] = ld_cluster_f2(mapa(la, (uint32_t)cr));
+                        M = fmaxf(M, pr[cr].x);
+                    }
+                }
+                float Z = 0.f;
+#pragma unroll
+                for (int cr = 0; cr < 8; ++cr)
+                    if (cr < ncta) Z += pr[cr].y * ex2(pr[cr].x - M);
+                lse[k] = M + log2f(Z);
+            }
+        }
+        cluster_arrive();
+        cluster_wait();
+        float *lse2 = reinterpret_cast<float *>(part);   // reuse: every peer is done reading
+#pragma unroll
+        for (int k = 0; k < kMaxRowsPerThread; ++k) {
+            const int r = sidx + k * kSoftThreads;
+            if (r < TT) lse2[r] = lse[k];
+        }
+        named_barrier(1, kSoftThreads);
+
+        // pass 2: column sums with keys on TMEM lanes
+        float acc = 0.f;
+        for (int t = 0; t < T2; ++t) {
+            const int j = T + t, b = j & 1;
+            wait_phase(smem_u32(&sh->tfull[b]), (j >> 1) & 1, sh, err);
+            tc_fence_after();
+            uint32_t v[4][32];
+            const bool mine = hf < nM;
+            if (mine) {
+                const uint32_t ta = tmem + lane_base + b * 256 + hf * 128;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tmem_ld32(ta + k * 32, v[k]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tmem_wait_ld(v[k]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+            if (mine) {
+                const float4 *l4 = reinterpret_cast<const float4 *>(lse2 + t * kStrip);
+                float ssum = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 q = l4[(k * 32 + i) >> 2];
+                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 0]), c2, -q.x));
+                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 1]), c2, -q.y));
+                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 2]), c2, -q.z));
+                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 3]), c2, -q.w));
+                    }
+                acc += ssum;
+            }
+        }
+        const int key = slice0 + hf * 128 + row;
+        if (hf < nM && key < g.C) scores[u * g.C + key] = acc;
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+template <int D>
+cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st)
+{
+    const int ncta = (g.W + kSlice - 1) / kSlice;
+    const int T = (g.G * g.W + kStrip - 1) / kStrip;
+    int stages = kMaxStages;
+    while (stages > 2 && smem_bytes(D, T, stages) > 232448) --stages;
+    const size_t smem = smem_bytes(D, T, stages);
+    if (smem > 232448) return cudaErrorInvalidValue;
+
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t rows = (cuuint64_t)g.n * g.layers * g.hq * g.W;
+    cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kStrip};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(g.q), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    auto kern = score_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(g.nwin * ncta));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ncta;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float c2 = 1.4426950408889634f / sqrtf((float)D);
+    return cudaLaunchKernelEx(&cfg, kern, tmap, g, scores, err, ncta, T, stages, c2);
+}
+
+}  // namespace
+
+size_t score_scratch_bytes(const Geo &) { return 0; }
+
+cudaError_t launch_score(const Geo &g, float *scores, void *, int32_t *err, cudaStream_t st)
+{
+    if (g.nwin == 0) return cudaSuccess;
+    if (g.G * g.W > 8192) return cudaErrorInvalidValue;
+    return g.D == 128 ? launch_tc<128>(g, scores, err, st) : launch_tc<64>(g, scores, err, st);
+}
+
+}  // namespace kara

@@ -32,8 +32,9 @@
  * p0 = floor(ws / bs), L' = L - C + R.
  *
  * Supported shapes: D in {64, 128}; block_size 16; 1 <= G <= 8;
- * W a multiple of 64 with 64 <= W <= 2048; 1 <= K <= min(C, 1024);
- * 1 <= R <= C.  Anything else returns KARA_EUNSUPPORTED or KARA_EINVAL.
+ * W a multiple of 64 with 64 <= W <= 2048 and G*W <= 8192;
+ * 1 <= K <= min(C, 1024); 1 <= R <= C.  Anything else returns
+ * KARA_EUNSUPPORTED or KARA_EINVAL.
  */
 #ifndef KARA_H
 #define KARA_H

@@ -99,6 +99,35 @@ def test_score_alone_matches_oracle():
     assert rel_err(scores.cpu().numpy(), ref).max() <= SCORE_RTOL
 
 
+SCORE_SHAPES = [
+    # (G, W, B, D): cluster sizes 1..8, partial last key slice, partial last query strip,
+    # CTAs with 0, 1 or 2 compressible tiles, both head dims
+    (2, 64, 16, 64), (1, 64, 8, 128), (3, 192, 40, 128), (2, 256, 32, 128), (5, 320, 72, 64),
+    (4, 512, 64, 128), (1, 640, 100, 128), (5, 1024, 128, 128), (8, 1024, 300, 64), (4, 2048, 256, 128),
+    (2, 1600, 700, 128),
+]
+
+
+@pytest.mark.parametrize("G,W,B,D", SCORE_SHAPES)
+def test_score_shapes(G, W, B, D):
+    kara = lib()
+    spec = random_spec(500 + W + G, G=G, hkv=2, W=W, B=B, D=D, n_seq=2, layers=1, len_lo=W, len_hi=W + 40,
+                       plant="bernoulli")
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    c = kara.cache(d.k, d.v, spec.hq)
+    p = kara.params(spec.W, spec.B, 1, 1, spec.lam)
+    b = kara.batch(d.lengths, d.block_table, d.q)
+    scores = torch.full((spec.n_seq, spec.layers, spec.hkv, spec.C), -1.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(kara.kara_workspace_size(c, p, spec.n_seq), 1), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_score(c, p, b, scores, ws, err)
+    assert kara.kara_get_error(err) == 0
+    ref = oracle.scores(oracle.shape_of(wl), wl.q, wl.k, wl.block_table, wl.lengths)
+    e = rel_err(scores.cpu().numpy(), ref)
+    assert e.max() <= SCORE_RTOL, f"max rel err {e.max():.3e} at {np.unravel_index(e.argmax(), e.shape)}"
+
+
 def test_compact_alone_with_oracle_kept():
     kara = lib()
     spec = random_spec(6, G=2, hkv=2, W=128, B=16, D=64, n_seq=3, layers=2, R=30, len_lo=128, len_hi=300)
