@@ -110,6 +110,77 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *e
     }
 }
 
+__device__ __forceinline__ float fv(uint32_t x) { return __uint_as_float(x); }
+
+// Max of 32 fp32 values (raw bits), a tree of 3-input max of depth 4.
+__device__ __forceinline__ float max32(const uint32_t (&v)[32])
+{
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) a[i] = max3(fv(v[3 * i]), fv(v[3 * i + 1]), fv(v[3 * i + 2]));
+    a[10] = fmaxf(fv(v[30]), fv(v[31]));
+    const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
+    return max3(max3(b0, b1, b2), a[9], a[10]);
+}
+
+// 2^y for a pair of values on the special-function unit.  (Sending a share of
+// the pairs to the FMA-pipe polynomial exp2_poly2 was measured slower here:
+// the exponential unit is not what bounds this kernel.)
+template <int SLOT>
+__device__ __forceinline__ uint64_t exp2_pair(uint64_t y)
+{
+    float y0, y1;
+    unpack2(y, y0, y1);
+    return pack2(ex2(y0), ex2(y1));
+}
+
+// acc[j] += 2^(x*c2 + nm) for 32 values, as 4 packed pairs of partial sums.
+__device__ __forceinline__ void exp_sum32(const uint32_t (&v)[32], uint64_t c2p, uint64_t nmp, uint64_t (&acc)[4])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const uint64_t y0 = fma2(pack2(fv(v[i + 0]), fv(v[i + 1])), c2p, nmp);
+        const uint64_t y1 = fma2(pack2(fv(v[i + 2]), fv(v[i + 3])), c2p, nmp);
+        const uint64_t y2 = fma2(pack2(fv(v[i + 4]), fv(v[i + 5])), c2p, nmp);
+        const uint64_t y3 = fma2(pack2(fv(v[i + 6]), fv(v[i + 7])), c2p, nmp);
+        acc[0] = add2(acc[0], exp2_pair<0>(y0));
+        acc[1] = add2(acc[1], exp2_pair<1>(y1));
+        acc[2] = add2(acc[2], exp2_pair<2>(y2));
+        acc[3] = add2(acc[3], exp2_pair<3>(y3));
+    }
+}
+
+// acc[j] += 2^(x_n*c2 + nl[n]) for the 32 columns n of one TMEM load; nl is 16-byte aligned.
+__device__ __forceinline__ void exp_sum32_cols(const uint32_t (&v)[32], uint64_t c2p, const float *nl,
+                                               uint64_t (&acc)[4])
+{
+    const float4 *n4 = reinterpret_cast<const float4 *>(nl);
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        const float4 qa = n4[i >> 2], qb = n4[(i >> 2) + 1];
+        const uint64_t y0 = fma2(pack2(fv(v[i + 0]), fv(v[i + 1])), c2p, pack2(qa.x, qa.y));
+        const uint64_t y1 = fma2(pack2(fv(v[i + 2]), fv(v[i + 3])), c2p, pack2(qa.z, qa.w));
+        const uint64_t y2 = fma2(pack2(fv(v[i + 4]), fv(v[i + 5])), c2p, pack2(qb.x, qb.y));
+        const uint64_t y3 = fma2(pack2(fv(v[i + 6]), fv(v[i + 7])), c2p, pack2(qb.z, qb.w));
+        acc[0] = add2(acc[0], exp2_pair<0>(y0));
+        acc[1] = add2(acc[1], exp2_pair<1>(y1));
+        acc[2] = add2(acc[2], exp2_pair<2>(y2));
+        acc[3] = add2(acc[3], exp2_pair<3>(y3));
+    }
+}
+
+__device__ __forceinline__ float sum_pairs(const uint64_t (&acc)[4])
+{
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float lo, hi;
+        unpack2(acc[j], lo, hi);
+        s += lo + hi;
+    }
+    return s;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
@@ -304,16 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                if (k < nld)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) m = fmaxf(m, __uint_as_float(v[k][i]));
+                if (k < nld) m = fmaxf(m, max32(v[k]));
             const float mc = m * c2;
-            float z = 0.f;
+            uint64_t acc[4] = {0, 0, 0, 0};
+            const uint64_t c2p = pack2(c2, c2), nmp = pack2(-mc, -mc);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                if (k < nld)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) z += ex2(fmaf(__uint_as_float(v[k][i]), c2, -mc));
+                if (k < nld) exp_sum32(v[k], c2p, nmp, acc);
+            const float z = sum_pairs(acc);
             if (hf == 1) xbuf[b * kStrip + row] = make_float2(mc, z);
             named_barrier(1, kSoftThreads);
             if (hf == 0) {
@@ -354,11 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cluster_arrive();
         cluster_wait();
-        float *lse2 = reinterpret_cast<float *>(part);   // reuse: every peer is done reading
+        // -lse2 per row, in place of the partials: every peer is done reading them
+        float *nlse2 = reinterpret_cast<float *>(part);
 #pragma unroll
         for (int k = 0; k < kMaxRowsPerThread; ++k) {
             const int r = sidx + k * kSoftThreads;
-            if (r < TT) lse2[r] = lse[k];
+            if (r < TT) nlse2[r] = -lse[k];
         }
         named_barrier(1, kSoftThreads);
 
@@ -381,19 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
             if (mine) {
-                const float4 *l4 = reinterpret_cast<const float4 *>(lse2 + t * kStrip);
-                float ssum = 0.f;
+                const float *nl = nlse2 + t * kStrip;
+                uint64_t pacc[4] = {0, 0, 0, 0};
+                const uint64_t c2p = pack2(c2, c2);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 q = l4[(k * 32 + i) >> 2];
-                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 0]), c2, -q.x));
-                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 1]), c2, -q.y));
-                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 2]), c2, -q.z));
-                        ssum += ex2(fmaf(__uint_as_float(v[k][i + 3]), c2, -q.w));
-                    }
-                acc += ssum;
+                for (int k = 0; k < 4; ++k) exp_sum32_cols(v[k], c2p, nl + k * 32, pacc);
+                acc += sum_pairs(pacc);
             }
         }
         const int key = slice0 + hf * 128 + row;

@@ -196,5 +196,82 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// ---- packed fp32 pairs and 3-input max ----------------------------------------
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t r, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+// (a*b + c) on both halves, round-to-nearest, one instruction.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// ---- 2^y on the FMA pipe ------------------------------------------------------
+// Cody-Waite style split y = n + f, n = round(y), |f| <= 1/2, and
+// 2^y = 2^f * 2^n.  2^f is a degree-4 polynomial whose coefficients come from
+// a Remez exchange that minimises the relative error on [-1/2, 1/2]; evaluated
+// in fp32 Horner form with fused multiply-adds its relative error stays below
+// 3e-6.  2^n is applied by adding n to the exponent field.  Inputs are clamped
+// at -126 so the exponent never underflows (2^-126 stands in for anything
+// smaller, as the flush-to-zero ex2 gives 0 there).  Used for a share of the
+// exponentials so that the special-function unit is not the only exp engine.
+constexpr float kExp2C0 = 0.99999928474426270f;
+constexpr float kExp2C1 = 0.69312179088592530f;
+constexpr float kExp2C2 = 0.24024744331836700f;
+constexpr float kExp2C3 = 0.05591785907745361f;
+constexpr float kExp2C4 = 0.00957010220736265f;
+
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t y2)
+{
+    const uint64_t round_magic = pack2(12582912.f, 12582912.f);  // 1.5 * 2^23
+    float y0, y1;
+    unpack2(y2, y0, y1);
+    const uint64_t y = pack2(fmaxf(y0, -126.f), fmaxf(y1, -126.f));
+    const uint64_t t = add2(y, round_magic);        // n sits in the low mantissa bits of t
+    const uint64_t f = sub2(y, sub2(t, round_magic));
+    uint64_t p = fma2(pack2(kExp2C4, kExp2C4), f, pack2(kExp2C3, kExp2C3));
+    p = fma2(p, f, pack2(kExp2C2, kExp2C2));
+    p = fma2(p, f, pack2(kExp2C1, kExp2C1));
+    p = fma2(p, f, pack2(kExp2C0, kExp2C0));
+    float p0, p1, t0, t1;
+    unpack2(p, p0, p1);
+    unpack2(t, t0, t1);
+    const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+    const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+    return pack2(r0, r1);
+}
+
 }  // namespace ptx
 }  // namespace kara
