@@ -204,6 +204,10 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     ap.add_argument("--profile-kernel", choices=["score", "select", "compact"], default=None,
                     help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
+    ap.add_argument("--sweep", action="store_true",
+                    help="periodic-policy sweep on the Qwen3-4B shape: one JSON line per compression event")
+    ap.add_argument("--sweep-batches", default="1,8,32,128,256")
+    ap.add_argument("--sweep-windows", default="128,256,512,1024,2048")
     args = ap.parse_args()
     ws_, rank, local = dist_setup()
     if args.impl == "reference":
@@ -218,6 +222,9 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.sweep:
+        run_sweep(args, dev)
+        return
     spec = synth.SPECS[args.config].with_(seed=synth.SPECS[args.config].seed + 97 * rank)
     if args.n_seq:
         spec = spec.with_(n_seq=args.n_seq)
@@ -361,6 +368,78 @@ def main():
     if ws_ > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_sweep(args, dev):
+    """Periodic policy on the Qwen3-4B shape: 512 decode steps per point; every
+    128 steps a seeded half of the sequences compresses its trailing window.
+    Each event reports the kara_compress_batch time (plan, scoring, selection,
+    compaction and table rewrite, CUDA events around the call) and the blocks
+    it released.  Points whose memory would exceed `cap` are reported skipped."""
+    import math
+    from decode_kv_cache_03_gb300 import Compressor
+    from decode_kv_cache_03_gb300.periodic import BlockPool, PeriodicSchedule, append_tokens, compress_selected
+    hbm, tf_burst, _, src = peaks()
+    cap = 0.8 * torch.cuda.get_device_properties(dev).total_memory
+    index = 0
+    for b in [int(x) for x in args.sweep_batches.split(",")]:
+        for W in [int(x) for x in args.sweep_windows.split(",")]:
+            spec = synth.sweep_spec(b, W, index)
+            index += 1
+            block_bytes = spec.layers * spec.hkv * spec.block * spec.d * 2 * 2
+            per_new = math.ceil((spec.block - 1 + spec.R + spec.B) / spec.block)
+            fresh_per_seq = per_new + 512 // spec.block + 4
+            m_max = math.ceil(b / 2)
+            need = (16 + b * (W // spec.block + 1 + fresh_per_seq)) * block_bytes \
+                + m_max * spec.layers * spec.hq * W * spec.d * 2
+            point = {"batch": b, "W": W, "B": spec.B, "K": spec.K, "R": spec.R}
+            if need > cap:
+                print(json.dumps({"sweep": dict(point, skipped=f"capacity: needs {need / 1e9:.0f} GB")}), flush=True)
+                continue
+            wl = synth.generate(spec, device=dev, with_q=False, alias_prefix=True, fresh_per_seq=fresh_per_seq)
+            gen = torch.Generator(device=dev).manual_seed(1000 + index)
+            q = torch.empty(m_max, spec.layers, spec.hq, W, spec.d, dtype=torch.bfloat16, device=dev)
+            for i in range(m_max):
+                q[i].copy_(torch.randn(spec.layers, spec.hq, W, spec.d, generator=gen, device=dev))
+            comp = Compressor(wl.k, wl.v, spec.hq, W, spec.B, spec.K, spec.R, spec.lam)
+            lengths = wl.lengths.cpu().tolist()
+            stride = wl.bt_stride + 512 // spec.block + 1
+            table = torch.full((b, stride), -1, dtype=torch.int32)
+            table[:, :wl.bt_stride] = wl.block_table.cpu()
+            pool = BlockPool(wl.fresh.cpu().tolist(), pinned=range(wl.prefix_pool))
+            sched = PeriodicSchedule(128, 0.5, W, seed=index)
+            event = 0
+            for step in range(1, 513):
+                before = list(lengths)
+                append_tokens(lengths, table, pool, spec.block)
+                blk = torch.tensor([int(table[s, before[s] // spec.block]) for s in range(b)], device=dev)
+                slot = torch.tensor([before[s] % spec.block for s in range(b)], device=dev)
+                wl.k[:, blk, :, slot] = torch.randn(b, spec.layers, spec.hkv, spec.d, generator=gen,
+                                                    device=dev).to(torch.bfloat16)
+                wl.v[:, blk, :, slot] = torch.randn(b, spec.layers, spec.hkv, spec.d, generator=gen,
+                                                    device=dev).to(torch.bfloat16)
+                if not sched.due(step):
+                    continue
+                seqs = sched.choose(lengths)
+                event += 1
+                if not seqs:
+                    continue
+                m = len(seqs)
+                sel_lengths = [lengths[s] for s in seqs]
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                freed, status = compress_selected(comp, seqs, lengths, table, q[:m], pool, events=ev)
+                torch.cuda.synchronize()
+                ms = ev[0].elapsed_time(ev[1])
+                sp = spec.with_(n_seq=m)
+                flops, sb, cb = algorithmic(sp, sel_lengths)
+                t_roof = max(flops / (tf_burst * 1e12), (sb + cb) / (hbm * 1e9))
+                nwin = m * spec.layers * spec.hkv
+                print(json.dumps({"sweep": dict(point, event=event, step=step, sequences=m, windows=nwin,
+                                                status=status, ms=ms, windows_per_s=nwin / (ms * 1e-3),
+                                                freed_blocks=len(freed), roofline_ms=t_roof * 1e3,
+                                                roofline_frac=t_roof / (ms * 1e-3), peaks=src)}), flush=True)
+            del wl, q, comp
+            torch.cuda.empty_cache()
 
 
 def launches_per_step():

@@ -14,6 +14,9 @@ import importlib
 _LAZY = {
     "kara": ("kara", None),
     "Compressor": ("compressor", "Compressor"),
+    "periodic": ("periodic", None),
+    "BlockPool": ("periodic", "BlockPool"),
+    "PeriodicSchedule": ("periodic", "PeriodicSchedule"),
     "KaraError": ("kara", "KaraError"),
     "kara_plan": ("kara", "kara_plan"),
     "kara_workspace_size": ("kara", "kara_workspace_size"),

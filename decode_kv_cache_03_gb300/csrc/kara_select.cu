@@ -190,10 +190,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R
 
     // 4. Visit order of the chunks: (score desc, left end asc).
     for (int t = tid; t < nch; t += kSelThreads) {
-        const float c = cs[t];
+        // order-preserving keys: the same order as the floats for finite
+        // scores, and a total order on every bit pattern, so the ranks always
+        // form a permutation (no index can go out of range on NaN input)
+        const uint32_t c = okey(cs[t]);
         int r = 0;
         for (int t2 = 0; t2 < nch; ++t2) {
-            const float c2 = cs[t2];
+            const uint32_t c2 = okey(cs[t2]);
             r += (c2 > c) || (c2 == c && t2 < t);
         }
         corder[r] = t;
@@ -239,11 +242,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R
     if (sh.count < R) {
         for (int t = tid; t < K; t += kSelThreads) {
             const int j = cand[t];
-            const float v = s[j];
+            const uint32_t v = okey(s[j]);
             int r = 0;
             for (int t2 = 0; t2 < K; ++t2) {
                 const int j2 = cand[t2];
-                const float v2 = s[j2];
+                const uint32_t v2 = okey(s[j2]);
                 r += (v2 > v) || (v2 == v && j2 < j);
             }
             corder2[r] = t;

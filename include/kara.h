@@ -145,7 +145,8 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
  *         positions, both in score order.
  *   kept: the R retained positions, ascending.
  * scores [n_windows][C], cand [n_windows][K] (may be NULL), kept [n_windows][R].
- * Scores must be finite; -0.0 is treated as +0.0.
+ * The order is the one stated for finite scores (-0.0 counts as +0.0); NaN
+ * scores still give a deterministic selection and never an out-of-range access.
  */
 kara_status kara_select(const kara_params *p, int64_t n_windows, const float *scores,
                         int32_t *cand, int32_t *kept, kara_stream_t stream);

@@ -170,8 +170,13 @@ def _plant_mask(spec: Spec, gen, device) -> torch.Tensor:
 
 
 def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
-             prefix_pool_blocks: int = 16) -> Workload:
-    """Draw one workload.  Deterministic for a given (spec, device type)."""
+             prefix_pool_blocks: int = 16, with_q: bool = True, extra_fresh_per_seq: int = 0,
+             fresh_per_seq: int | None = None) -> Workload:
+    """Draw one workload.  Deterministic for a given (spec, device type).
+
+    with_q=False leaves q as None (a caller that draws query windows itself);
+    fresh_per_seq sets the pool of unused blocks per sequence (default: a
+    window's worth, W/16 + 1) and extra_fresh_per_seq adds to it."""
     dev = torch.device(device)
     gen = _gen(spec.seed, dev)
     n, Lyr, Hq, Hk, D, bs, W = (spec.n_seq, spec.layers, spec.hq, spec.hkv, spec.d,
@@ -194,7 +199,7 @@ def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
     P = prefix_pool_blocks if alias_prefix else 0
     distinct_counts = [min(nb, tail) if alias_prefix else nb for nb in nblk_seq]
     Nd = sum(distinct_counts)
-    per_seq_fresh = W // bs + 1
+    per_seq_fresh = (W // bs + 1 if fresh_per_seq is None else fresh_per_seq) + extra_fresh_per_seq
     n_fresh = n * per_seq_fresh
     num_blocks = P + Nd + n_fresh
     host_gen = _gen(spec.seed + 2000, "cpu")
@@ -224,7 +229,7 @@ def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
 
     # window keys with structure, written through the block table
     u = _unit_dirs(Lyr, Hk, D, gen, dev)
-    q = torch.empty(n, Lyr, Hq, W, D, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(n, Lyr, Hq, W, D, dtype=torch.bfloat16, device=dev) if with_q else None
     bt_dev = bt.to(dev)
     planted_q = spec.plant in ("count", "bernoulli", "spans")
     for s in range(n):
@@ -242,6 +247,8 @@ def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
             m = _plant_mask(spec, gen, dev)
             kw = kw + 3.0 * m[..., None] * u[:, :, None, :]
         k[:, blk, :, slot, :] = kw.permute(2, 0, 1, 3).to(torch.bfloat16)
+        if not with_q:
+            continue
         qs = torch.randn(Lyr, Hq, W, D, generator=gen, device=dev)
         if planted_q:
             uq = u.repeat_interleave(G, dim=1)          # [layers][hq][D]

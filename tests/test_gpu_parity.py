@@ -82,6 +82,23 @@ def test_select_bitexact_with_ties(seed):
     assert np.array_equal(kept.cpu().numpy(), k_o)
 
 
+def test_select_stays_in_range_on_nan_scores():
+    """NaN scores have no order to follow, but the result must still be a valid selection."""
+    kara = lib()
+    rng = np.random.default_rng(3)
+    W, B, K, R, nwin = 1024, 128, 128, 268, 23
+    C = W - B
+    s = rng.random((nwin, C)).astype(np.float32)
+    s[rng.random(s.shape) < 0.3] = np.nan
+    s[0] = np.nan
+    cand = torch.empty(nwin, K, dtype=torch.int32, device="cuda")
+    kept = torch.empty(nwin, R, dtype=torch.int32, device="cuda")
+    kara.kara_select(kara.params(W, B, K, R, 0.1), nwin, torch.from_numpy(s).cuda(), cand, kept)
+    torch.cuda.synchronize()
+    for arr, n in ((cand.cpu().numpy(), K), (kept.cpu().numpy(), R)):
+        assert arr.shape[1] == n and np.all(np.diff(arr, axis=1) > 0) and arr.min() >= 0 and arr.max() < C
+
+
 def test_score_alone_matches_oracle():
     kara = lib()
     spec = random_spec(5, G=4, hkv=2, W=256, B=32, D=128, n_seq=2, layers=2, len_lo=300, len_hi=700)
