@@ -41,6 +41,24 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def measured_traffic(nwin):
+    """DRAM bytes of one scoring launch from the committed ncu capture, scaled by
+    windows; None when the scorer's sources changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "score_tc_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != rec["sources_sha256_16"]:
+            return None
+        return rec["bytes_per_window"] * nwin
+    except Exception:
+        return None
+
+
 def algorithmic(spec, lengths):
     """Per-step algorithmic work: QK^T FLOPs of the scoring and minimum bytes.
 
@@ -339,7 +357,9 @@ def main():
                    "step": "block table restored by a device copy, then kara_compress_batch",
                    "parallelism": f"dp{ws_} (independent batches per GPU)"},
         "roofline": {"bound": "tensor", "achieved": achieved_tflops, "peak": tf_sus, "unit": "TFLOP/s",
-                     "frac": achieved_tflops / tf_sus, "traffic": None,
+                     "frac": achieved_tflops / tf_sus, "traffic": measured_traffic(nwin),
+                     "traffic_unit": "bytes per launch (DRAM read + write)",
+                     "algorithmic_bytes": score_bytes,
                      "kernel": "window scoring (QK^T, softmax, column sums)",
                      "peak_kind": f"{src} sustained bf16", "frac_vs_burst": achieved_tflops / tf_burst},
         "phases_ms": {"score": score_ms, "select": select_ms, "compact_commit": compact_ms,
