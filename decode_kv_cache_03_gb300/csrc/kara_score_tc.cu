@@ -181,6 +181,42 @@ __device__ __forceinline__ float sum_pairs(const uint64_t (&acc)[4])
     return s;
 }
 
+// Merges the per-slice (max, sum of 2^(x - max)) pairs of query rows
+// r0, r0 + 256, ... below r_hi over the cluster's ncta slices and stores
+// -lse2 = -(max + log2 sum) into the .x field of the row's pair in every CTA.
+// NR rows at a time, all NR * ncta remote loads in flight before any is used.
+template <int NR, int NP>
+__device__ __forceinline__ void merge_rows(uint32_t part_u32, int r0, int r_hi, int ncta)
+{
+    for (; r0 < r_hi; r0 += NR * kSoftThreads) {
+        float2 pr[NR][NP];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            const int r = r0 + k * kSoftThreads;
+#pragma unroll
+            for (int cr = 0; cr < NP; ++cr)
+                if (r < r_hi && cr < ncta) pr[k][cr] = ld_cluster_f2(mapa(part_u32 + 8u * r, (uint32_t)cr));
+        }
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            const int r = r0 + k * kSoftThreads;
+            if (r >= r_hi) continue;
+            float M = -INFINITY;
+#pragma unroll
+            for (int cr = 0; cr < NP; ++cr)
+                if (cr < ncta) M = fmaxf(M, pr[k][cr].x);
+            float Z = 0.f;
+#pragma unroll
+            for (int cr = 0; cr < NP; ++cr)
+                if (cr < ncta) Z += pr[k][cr].y * ex2(pr[k][cr].x - M);
+            const float nl = -(M + log2f(Z));
+#pragma unroll
+            for (int cr = 0; cr < NP; ++cr)
+                if (cr < ncta) st_cluster_f32(mapa(part_u32 + 8u * r, (uint32_t)cr), nl);
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
@@ -396,39 +432,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         cluster_arrive();
         cluster_wait();
-        // merge the slices' (max, sum) of every query row across the cluster
+        // merge the slices' (max, sum) pairs of every query row: this CTA owns
+        // rows [r_lo, r_hi), reads their pairs from every peer and writes
+        // -lse2 into the .x field of the row's pair in every peer
         const int TT = T * kStrip;
-        float lse[kMaxRowsPerThread];
-#pragma unroll
-        for (int k = 0; k < kMaxRowsPerThread; ++k) {
-            const int r = sidx + k * kSoftThreads;
-            lse[k] = INFINITY;
-            if (r < GW) {
-                float2 pr[8];
-                float M = -INFINITY;
-                const uint32_t la = smem_u32(&part[r]);
-#pragma unroll
-                for (int cr = 0; cr < 8; ++cr) {
-                    if (cr < ncta) {
-                        pr[cr] = ld_cluster_f2(mapa(la, (uint32_t)cr));
-                        M = fmaxf(M, pr[cr].x);
-                    }
-                }
-                float Z = 0.f;
-#pragma unroll
-                for (int cr = 0; cr < 8; ++cr)
-                    if (cr < ncta) Z += pr[cr].y * ex2(pr[cr].x - M);
-                lse[k] = M + log2f(Z);
-            }
+        {
+            const int P = (GW + ncta - 1) / ncta;
+            const int r_lo = min(GW, (int)crank * P), r_hi = min(GW, r_lo + P);
+            const uint32_t pa = smem_u32(part);
+            if (ncta <= 4)
+                merge_rows<8, 4>(pa, r_lo + sidx, r_hi, ncta);
+            else
+                merge_rows<4, 8>(pa, r_lo + sidx, r_hi, ncta);
         }
         cluster_arrive();
         cluster_wait();
-        // -lse2 per row, in place of the partials: every peer is done reading them
+        // -lse2 of every row, packed to one float per row in place of the pairs;
+        // rows past G*W (the padding of the last strip) get -inf, so they add 0
+        float nlv[kMaxRowsPerThread];
+#pragma unroll
+        for (int k = 0; k < kMaxRowsPerThread; ++k) {
+            const int r = sidx + k * kSoftThreads;
+            nlv[k] = r < GW ? part[r].x : -INFINITY;
+        }
+        named_barrier(1, kSoftThreads);
         float *nlse2 = reinterpret_cast<float *>(part);
 #pragma unroll
         for (int k = 0; k < kMaxRowsPerThread; ++k) {
             const int r = sidx + k * kSoftThreads;
-            if (r < TT) nlse2[r] = -lse[k];
+            if (r < TT) nlse2[r] = nlv[k];
         }
         named_barrier(1, kSoftThreads);
 
