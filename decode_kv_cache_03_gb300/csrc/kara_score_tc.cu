@@ -17,10 +17,11 @@
 // rows through a TMA ring of 128-row strips, twice:
 //
 //   pass 1  S = Q_strip * K_slice^T  (M = 128 query rows, N = slice) into TMEM;
-//           per row the slice's max and sum of exponentials (fp32);
-//           the cluster then merges the slices' (max, sum) pairs through
-//           distributed shared memory into lse2[row] = log2 sum_j 2^(l2_j),
-//           l2 = <q,k> * log2(e)/sqrt(D).
+//           each half of the softmax warps takes half of the slice's keys
+//           and keeps, per row, the log2 of its sum of 2^l2 (fp32, shifted
+//           by its maximum); the cluster then merges these 2*ncta partials
+//           through distributed shared memory into
+//           lse2[row] = log2 sum_j 2^(l2_j), l2 = <q,k> * log2(e)/sqrt(D).
 //   pass 2  S^T = K_tile * Q_strip^T (M = 128 keys of the slice's compressible
 //           part, N = 128 query rows): key rows sit on TMEM lanes, so each
 //           thread owns one key and sums 2^(l2 - lse2[row]) over its row of
@@ -85,7 +86,7 @@ constexpr size_t kMinSmem = 120 * 1024;
 size_t smem_bytes(int D, int T, int stages)
 {
     const size_t kb = (size_t)kSlice * D * 2, qb = (size_t)kStrip * D * 2;
-    const size_t need = 1024 + kb + stages * qb + (size_t)T * kStrip * 8 + 2 * kStrip * 8 + sizeof(Shared);
+    const size_t need = 1024 + kb + stages * qb + (size_t)T * kStrip * 8 + sizeof(Shared);
     return need > kMinSmem ? need : kMinSmem;
 }
 
@@ -181,10 +182,11 @@ __device__ __forceinline__ float sum_pairs(const uint64_t (&acc)[4])
     return s;
 }
 
-// Merges the per-slice (max, sum of 2^(x - max)) pairs of query rows
-// r0, r0 + 256, ... below r_hi over the cluster's ncta slices and stores
-// -lse2 = -(max + log2 sum) into the .x field of the row's pair in every CTA.
-// NR rows at a time, all NR * ncta remote loads in flight before any is used.
+// Merges the per-half-slice log2-sum-exp pairs of query rows r0, r0 + 256,
+// ... below r_hi over the cluster's ncta slices and stores
+// -lse2 = -log2 sum 2^(l - max) - max into the .x field of the row's pair in
+// every CTA.  NR rows at a time, all NR * ncta remote loads in flight before
+// any is used.
 template <int NR, int NP>
 __device__ __forceinline__ void merge_rows(uint32_t part_u32, int r0, int r_hi, int ncta)
 {
@@ -204,16 +206,55 @@ __device__ __forceinline__ void merge_rows(uint32_t part_u32, int r0, int r_hi, 
             float M = -INFINITY;
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (cr < ncta) M = fmaxf(M, pr[k][cr].x);
+                if (cr < ncta) M = max3(M, pr[k][cr].x, pr[k][cr].y);
             float Z = 0.f;
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (cr < ncta) Z += pr[k][cr].y * ex2(pr[k][cr].x - M);
+                if (cr < ncta) Z += ex2(pr[k][cr].x - M) + ex2(pr[k][cr].y - M);
             const float nl = -(M + log2f(Z));
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
                 if (cr < ncta) st_cluster_f32(mapa(part_u32 + 8u * r, (uint32_t)cr), nl);
         }
+    }
+}
+
+// Pass 1 of one softmax thread (query row `row` of every strip, the
+// NLD * 32 keys of its warp half): for each strip, waits for the S tile in
+// TMEM buffer t & 1, releases the buffer once its columns are in registers,
+// and stores log2 sum 2^l2 over those keys (shifted by their maximum) at
+// lse_half[2 * r + hf].  NLD is a template parameter so that one strip's
+// loads, maxima and exponentials form a single branch-free block.
+template <int NLD>
+__device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta0, int row, int hf, int T, int GW,
+                                           float c2, float *lse_half)
+{
+    const int lane = threadIdx.x & 31;
+    for (int t = 0; t < T; ++t) {
+        const int b = t & 1;
+        wait_phase(smem_u32(&sh->tfull[b]), (t >> 1) & 1, sh, err);
+        tc_fence_after();
+        uint32_t v[NLD][32];
+#pragma unroll
+        for (int k = 0; k < NLD; ++k) tmem_ld32(ta0 + b * 256 + k * 32, v[k]);
+#pragma unroll
+        for (int k = 0; k < NLD; ++k) tmem_wait_ld(v[k]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+        float m = max32(v[0]);
+#pragma unroll
+        for (int k = 1; k < NLD; ++k) m = fmaxf(m, max32(v[k]));
+        const float mc = m * c2;
+        uint64_t acc[4] = {0, 0, 0, 0};
+        const uint64_t c2p = pack2(c2, c2), nmp = pack2(-mc, -mc);
+#pragma unroll
+        for (int k = 0; k < NLD; ++k) exp_sum32(v[k], c2p, nmp, acc);
+        const float z = sum_pairs(acc);
+        // z >= 1, as the maximum contributes 2^0.  The two halves of a row stay
+        // separate until the cluster merge, so no warp waits for another here.
+        const int r = t * kStrip + row;
+        if (r < GW) lse_half[2 * r + hf] = mc + log2f(z);
     }
 }
 
@@ -228,9 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sK = base;
     uint8_t *sQ = sK + C_::kKBytes;
-    float2 *part = reinterpret_cast<float2 *>(sQ + stages * C_::kQBytes);
-    float2 *xbuf = part + T * kStrip;                       // [2][128]
-    Shared *sh = reinterpret_cast<Shared *>(xbuf + 2 * kStrip);
+    float2 *part = reinterpret_cast<float2 *>(sQ + stages * C_::kQBytes);  // per row: the two halves' lse2
+    Shared *sh = reinterpret_cast<Shared *>(part + T * kStrip);
     const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -390,51 +430,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * q4 + lane;
         const int sidx = (warp - 2) * 32 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        const int half = S >> 1, nld = half >> 5;  // 1..4 loads of 32 columns
+        const int nld = S >> 6;  // loads of 32 columns per warp half: 1..4
 
-        // pass 1: row max and sum of exponentials over this CTA's keys
-        for (int t = 0; t < T; ++t) {
-            const int b = t & 1;
-            wait_phase(smem_u32(&sh->tfull[b]), (t >> 1) & 1, sh, err);
-            tc_fence_after();
-            uint32_t v[4][32];
-            const uint32_t ta = tmem + lane_base + b * 256 + hf * half;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < nld) tmem_ld32(ta + k * 32, v[k]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < nld) tmem_wait_ld(v[k]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
-            float m = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < nld) m = fmaxf(m, max32(v[k]));
-            const float mc = m * c2;
-            uint64_t acc[4] = {0, 0, 0, 0};
-            const uint64_t c2p = pack2(c2, c2), nmp = pack2(-mc, -mc);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < nld) exp_sum32(v[k], c2p, nmp, acc);
-            const float z = sum_pairs(acc);
-            if (hf == 1) xbuf[b * kStrip + row] = make_float2(mc, z);
-            named_barrier(1, kSoftThreads);
-            if (hf == 0) {
-                const float2 o = xbuf[b * kStrip + row];
-                const float M = fmaxf(mc, o.x);
-                const float Z = z * ex2(mc - M) + o.y * ex2(o.x - M);
-                const int r = t * kStrip + row;
-                if (r < GW) part[r] = make_float2(M, Z);
-            }
+        // pass 1: per row, log2-sum-exp over this warp half's keys of the slice
+        float *lse_half = reinterpret_cast<float *>(part);
+        switch (nld) {
+        case 1: pass1_rows<1>(sh, err, tmem + lane_base + hf * 32, row, hf, T, GW, c2, lse_half); break;
+        case 2: pass1_rows<2>(sh, err, tmem + lane_base + hf * 64, row, hf, T, GW, c2, lse_half); break;
+        case 3: pass1_rows<3>(sh, err, tmem + lane_base + hf * 96, row, hf, T, GW, c2, lse_half); break;
+        default: pass1_rows<4>(sh, err, tmem + lane_base + hf * 128, row, hf, T, GW, c2, lse_half); break;
         }
         __syncwarp();
         cluster_arrive();
         cluster_wait();
-        // merge the slices' (max, sum) pairs of every query row: this CTA owns
-        // rows [r_lo, r_hi), reads their pairs from every peer and writes
-        // -lse2 into the .x field of the row's pair in every peer
+        // merge the half-slices' lse2 of every query row: this CTA owns rows
+        // [r_lo, r_hi), reads their pairs from every peer and writes -lse2 into
+        // the .x field of the row's pair in every peer
         const int TT = T * kStrip;
         {
             const int P = (GW + ncta - 1) / ncta;
