@@ -178,6 +178,13 @@ def max_over_ranks(x, ws):
     return float(t.item())
 
 
+def sample_layers(wl, seqs, target_s=12.0):
+    """Layers of the oracle sample: enough for about target_s seconds of host
+    work (timed from a one-layer probe), at most the workload's layer count."""
+    _, dt, _, _ = cpu_oracle_sample(wl, seqs, 1)
+    return max(1, min(wl.spec.layers, int(round(target_s / max(dt, 1e-3)))))
+
+
 def run_reference(args, ws, rank):
     """The oracle arm: each step is a bounded sample of the workload on the host cores."""
     if rank != 0:
@@ -186,8 +193,8 @@ def run_reference(args, ws, rank):
     oracle.build()
     spec = synth.SPECS[args.config]
     seqs = list(range(min(2, spec.n_seq)))
-    layers_sample = 1
-    wl = synth.generate(spec.with_(n_seq=len(seqs), layers=layers_sample), device="cpu")
+    wl = synth.generate(spec.with_(n_seq=len(seqs)), device="cpu")
+    layers_sample = sample_layers(wl, seqs)
     for _ in range(args.warmup):
         cpu_oracle_sample(wl, seqs, layers_sample)
     times = []
@@ -202,7 +209,7 @@ def run_reference(args, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{args.config}: oracle sample of {nwin} windows "
-                                   f"({len(seqs)} sequences x {layers_sample} layer x {spec.hkv} KV heads)"},
+                                   f"({len(seqs)} sequences x {layers_sample} layers x {spec.hkv} KV heads)"},
             "cpu_baseline": {"value": val, "unit": "windows/s", "cores": thr, "kind": "oracle",
                              "sample": f"{nwin} windows of the {args.config} workload per step"},
             "e2e": {"value": val, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -379,9 +386,10 @@ def main():
         sample_seqs = list(range(min(2, spec.n_seq)))
         bt.copy_(bt0)
         torch.cuda.synchronize()
-        rate, dt, thr, sw = cpu_oracle_sample(wl, sample_seqs, 1)
+        nl = sample_layers(wl, sample_seqs)
+        rate, dt, thr, sw = cpu_oracle_sample(wl, sample_seqs, nl)
         line["cpu_baseline"] = {"value": rate, "unit": "windows/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{sw} windows ({len(sample_seqs)} sequences x 1 layer x "
+                                "sample": f"{sw} windows ({len(sample_seqs)} sequences x {nl} layers x "
                                           f"{spec.hkv} KV heads) of the same workload, {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
