@@ -51,6 +51,11 @@ def lib():
         _lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         _lib.kro_scores.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, ctypes.c_int]
+        _lib.kro_scores_causal.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, ctypes.c_int]
+        _lib.kro_select_mode.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_float, P, P, P]
+        _lib.kro_select_mode_batch.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P, P, ctypes.c_int]
         _lib.kro_select.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                     P, P, P, P, P]
         _lib.kro_select_batch.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -106,8 +111,9 @@ def shape_of(wl) -> Shape:
                       wl.bt_stride, wl.num_blocks)
 
 
-def scores(shape: Shape, q, kpool, block_table, lengths, with_colsum=False, nthreads=None):
-    """fp32 scores [n_seq][layers][hkv][C] (and fp64 full column sums [.., W])."""
+def scores(shape: Shape, q, kpool, block_table, lengths, with_colsum=False, nthreads=None, causal=False):
+    """fp32 scores [n_seq][layers][hkv][C] (and fp64 full column sums [.., W]).
+    causal=True: the unidirectional scoring ablation (kro_scores_causal)."""
     qa = _np(q, np.uint16)
     ka = _np(kpool, np.uint16)
     bt = _np(block_table, np.int32)
@@ -115,8 +121,9 @@ def scores(shape: Shape, q, kpool, block_table, lengths, with_colsum=False, nthr
     C = shape.W - shape.B
     out = np.zeros((shape.n_seq, shape.layers, shape.hkv, C), dtype=np.float32)
     cs = np.zeros((shape.n_seq, shape.layers, shape.hkv, shape.W), dtype=np.float64) if with_colsum else None
-    st = lib().kro_scores(ctypes.byref(shape), _ptr(qa), _ptr(ka), _ptr(bt), _ptr(ln), _ptr(out),
-                          _ptr(cs) if cs is not None else None, int(nthreads or max_threads()))
+    fn = lib().kro_scores_causal if causal else lib().kro_scores
+    st = fn(ctypes.byref(shape), _ptr(qa), _ptr(ka), _ptr(bt), _ptr(ln), _ptr(out),
+            _ptr(cs) if cs is not None else None, int(nthreads or max_threads()))
     if st != OK:
         raise ValueError(f"oracle scores failed: status {st}")
     return (out, cs) if with_colsum else out
@@ -149,6 +156,37 @@ def select_batch(scores_arr, K: int, R: int, lam: float, nthreads=None):
     kept = np.zeros(lead + (R,), np.int32)
     st = lib().kro_select_batch(nwin, C, K, R, ctypes.c_float(lam), _ptr(sa), _ptr(cand),
                                 _ptr(kept), int(nthreads or max_threads()))
+    if st != OK:
+        raise ValueError(f"oracle select failed: status {st}")
+    return cand, kept
+
+
+SELECT_TOKEN2CHUNK, SELECT_TOP_R, SELECT_FIXED_CHUNK = 0, 1, 2
+
+
+def select_mode(s, K: int, R: int, lam: float, mode: int, chunk: int = 0):
+    """One window under selection mode 0 (Token2Chunk), 1 (token Top-R) or 2
+    (fixed chunks of `chunk` tokens): cand[K], kept[R]."""
+    sa = _np(s, np.float32).reshape(-1)
+    cand = np.zeros(K, np.int32)
+    kept = np.zeros(R, np.int32)
+    st = lib().kro_select_mode(int(mode), int(chunk), sa.shape[0], K, R, ctypes.c_float(lam), _ptr(sa),
+                               _ptr(cand), _ptr(kept))
+    if st != OK:
+        raise ValueError(f"oracle select failed: status {st}")
+    return cand, kept
+
+
+def select_mode_batch(scores_arr, K: int, R: int, lam: float, mode: int, chunk: int = 0, nthreads=None):
+    """scores [..., C] -> cand [..., K], kept [..., R] under a selection mode."""
+    sa = _np(scores_arr, np.float32)
+    lead = sa.shape[:-1]
+    C = sa.shape[-1]
+    nwin = int(np.prod(lead)) if lead else 1
+    cand = np.zeros(lead + (K,), np.int32)
+    kept = np.zeros(lead + (R,), np.int32)
+    st = lib().kro_select_mode_batch(int(mode), int(chunk), nwin, C, K, R, ctypes.c_float(lam), _ptr(sa),
+                                     _ptr(cand), _ptr(kept), int(nthreads or max_threads()))
     if st != OK:
         raise ValueError(f"oracle select failed: status {st}")
     return cand, kept

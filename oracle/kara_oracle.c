@@ -12,8 +12,10 @@
  * 2607.01237) -- its abstract and Section 1 -- and the gist.science technical
  * summary of that paper, sections "1. Sliding-Window Bidirectional Attention
  * Scoring", "2. Token2Chunk Module" and "3. KvLLM Framework and Periodic
- * Compression".  The pages give no formula; every reading taken where they
- * are silent is named at the function that takes it.
+ * Compression"; the ablation variants (causal scores, token-level Top-R,
+ * fixed-size chunks) follow its "Experimental Results" (ablation studies) and
+ * "Problem Statement" (item 2).  The pages give no formula; every reading
+ * taken where they are silent is named at the function that takes it.
  *
  * Notation, per window u = (sequence s, layer l, KV head g):
  *   L  cached length, W window, ws = L - W window start (logical position),
@@ -99,9 +101,8 @@ static const uint16_t *pool_row(const kro_shape *sh, const uint16_t *pool, const
  * q: bf16 bits [n_seq][layers][hq][W][d]; kpool: bf16 bits, strides in sh;
  * scores: [n_seq][layers][hkv][C]; colsum (optional): [n_seq][layers][hkv][W].
  */
-int kro_scores(const kro_shape *sh, const uint16_t *q, const uint16_t *kpool,
-               const int32_t *bt, const int32_t *len, float *scores, double *colsum,
-               int nthreads)
+static int scores_impl(const kro_shape *sh, int causal, const uint16_t *q, const uint16_t *kpool,
+                       const int32_t *bt, const int32_t *len, float *scores, double *colsum, int nthreads)
 {
     const int W = sh->W, C = sh->W - sh->B, D = sh->d;
     const int G = sh->hq / sh->hkv;
@@ -135,16 +136,17 @@ int kro_scores(const kro_shape *sh, const uint16_t *q, const uint16_t *kpool,
                 for (int i = 0; i < W; ++i) {
                     const uint16_t *qrow = q + ((((int64_t)s * sh->layers + l) * sh->hq + h) * W + i) * D;
                     for (int e = 0; e < D; ++e) qd[e] = bf16_to_double(qrow[e]);
+                    const int nk = causal ? i + 1 : W;  /* keys this query attends to */
                     double m = -INFINITY;
-                    for (int j = 0; j < W; ++j) {
+                    for (int j = 0; j < nk; ++j) {
                         double acc = 0.0;
                         for (int e = 0; e < D; ++e) acc += qd[e] * kd[(size_t)j * D + e];
                         lg[j] = sigma * acc;
                         if (lg[j] > m) m = lg[j];
                     }
                     double Z = 0.0;
-                    for (int j = 0; j < W; ++j) Z += exp(lg[j] - m);
-                    for (int j = 0; j < W; ++j) t[j] += exp(lg[j] - m) / Z;
+                    for (int j = 0; j < nk; ++j) Z += exp(lg[j] - m);
+                    for (int j = 0; j < nk; ++j) t[j] += exp(lg[j] - m) / Z;
                 }
             }
             for (int j = 0; j < C; ++j) scores[u * C + j] = (float)t[j];
@@ -157,6 +159,29 @@ int kro_scores(const kro_shape *sh, const uint16_t *q, const uint16_t *kpool,
         free(kd); free(qd); free(lg); free(t);
     }
     return status;
+}
+
+int kro_scores(const kro_shape *sh, const uint16_t *q, const uint16_t *kpool, const int32_t *bt,
+               const int32_t *len, float *scores, double *colsum, int nthreads)
+{
+    return scores_impl(sh, 0, q, kpool, bt, len, scores, colsum, nthreads);
+}
+
+/*
+ * Causal window scores: the ablation that removes bidirectional scoring
+ * (summary, "Experimental Results", ablation studies: removing the
+ * bidirectional attention scoring costs accuracy).  Reading: without it, each
+ * window query attends as in decoding, to the window keys at or before its own
+ * position only:
+ *     p[j] = exp(l[j] - max) / sum_{j' <= i} exp(l[j'] - max)  for j <= i,
+ *     p[j] = 0                                                 for j >  i,
+ * with max over j <= i; everything else is as in kro_scores (so still
+ * sum_{j<W} t[j] = G*W).
+ */
+int kro_scores_causal(const kro_shape *sh, const uint16_t *q, const uint16_t *kpool, const int32_t *bt,
+                      const int32_t *len, float *scores, double *colsum, int nthreads)
+{
+    return scores_impl(sh, 1, q, kpool, bt, len, scores, colsum, nthreads);
 }
 
 /* ---- selection ---------------------------------------------------------- */
@@ -288,6 +313,93 @@ int kro_select(int C, int K, int R, float lambda, const float *s, int32_t *cand,
 
     free(order); free(tmp); free(in); free(cs); free(ca); free(corder);
     return w == R ? KRO_OK : KRO_EINVAL;
+}
+
+/*
+ * The two selection ablations.  Both keep the Top-K candidates (cand) of
+ * kro_select and replace Token2Chunk:
+ *
+ * mode 1, token-level Top-R -- the ablation that removes Token2Chunk (summary,
+ *   "Experimental Results", ablation studies), leaving isolated KV pairs
+ *   (summary, "Problem Statement", item 2): kept = the R positions first in
+ *   the score order, sorted by index.
+ *
+ * mode 2, fixed-size chunks with rigid boundaries (summary, "Problem
+ *   Statement", item 2, the granularity Token2Chunk replaces).  Readings: the
+ *   compressible region is cut into chunks [k*chunk, min(C, (k+1)*chunk)); a
+ *   chunk scores the mean of its scores, summed in float in index order and
+ *   divided by its length (round to nearest); chunks are visited by (mean
+ *   desc, start asc) and kept whole when they fit the budget (first fit); the
+ *   budget is then filled to exactly R with any other position in score order,
+ *   as kro_select does.
+ *
+ * mode 0 is kro_select.  chunk is used by mode 2 only (1 <= chunk <= C).
+ */
+int kro_select_mode(int mode, int chunk, int C, int K, int R, float lambda, const float *s, int32_t *cand,
+                    int32_t *kept)
+{
+    if (mode == 0) return kro_select(C, K, R, lambda, s, cand, kept, NULL, NULL);
+    if (mode < 0 || mode > 2 || C < 1 || K < 1 || K > C || R < 1 || R > C) return KRO_EINVAL;
+    if (mode == 2 && (chunk < 1 || chunk > C)) return KRO_EINVAL;
+    int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)C);
+    int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)C);
+    uint8_t *in = (uint8_t *)calloc((size_t)C, 1);
+    for (int j = 0; j < C; ++j) order[j] = j;
+    merge_sort(order, tmp, C, first_by_score, s);
+    for (int t = 0; t < K; ++t) cand[t] = order[t];
+    merge_sort(cand, tmp, K, first_ascending, NULL);
+
+    int count = 0;
+    if (mode == 2) {
+        const int nch = (C + chunk - 1) / chunk;
+        float *mean = (float *)malloc(sizeof(float) * (size_t)nch);
+        int32_t *start = (int32_t *)malloc(sizeof(int32_t) * (size_t)nch);
+        int32_t *corder = (int32_t *)malloc(sizeof(int32_t) * (size_t)nch);
+        int32_t *ctmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)nch);
+        for (int k = 0; k < nch; ++k) {
+            const int a = k * chunk, b = (k + 1) * chunk < C ? (k + 1) * chunk : C;
+            float sum = 0.0f;
+            for (int j = a; j < b; ++j) sum += s[j];
+            mean[k] = sum / (float)(b - a);
+            start[k] = a;
+            corder[k] = k;
+        }
+        chunk_ctx cc = { mean, start };
+        merge_sort(corder, ctmp, nch, first_chunk, &cc);
+        for (int r = 0; r < nch; ++r) {
+            const int k = corder[r];
+            const int a = k * chunk, b = (k + 1) * chunk < C ? (k + 1) * chunk : C;
+            if (count + (b - a) <= R) {
+                for (int j = a; j < b; ++j) in[j] = 1;
+                count += b - a;
+            }
+        }
+        free(mean); free(start); free(corder); free(ctmp);
+    }
+    for (int r = 0; r < C && count < R; ++r)
+        if (!in[order[r]]) { in[order[r]] = 1; ++count; }
+    int w = 0;
+    for (int j = 0; j < C; ++j)
+        if (in[j]) kept[w++] = j;
+    free(order); free(tmp); free(in);
+    return w == R ? KRO_OK : KRO_EINVAL;
+}
+
+/* kro_select_mode over nwin windows laid out back to back. */
+int kro_select_mode_batch(int mode, int chunk, int64_t nwin, int C, int K, int R, float lambda,
+                          const float *scores, int32_t *cand, int32_t *kept, int nthreads)
+{
+    int status = KRO_OK;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
+    for (int64_t u = 0; u < nwin; ++u) {
+        int st = kro_select_mode(mode, chunk, C, K, R, lambda, scores + u * C, cand + u * K, kept + u * R);
+        if (st != KRO_OK) {
+#pragma omp atomic write
+            status = st;
+        }
+    }
+    return status;
 }
 
 /* kro_select over nwin windows laid out back to back: scores [nwin][C],

@@ -44,8 +44,9 @@ def random_spec(seed, G=2, hkv=2, W=64, B=16, D=64, block=16, n_seq=2, layers=2,
                       shuffled, plant, 0.05, seed)
 
 
-def independent_colsum(wl):
-    """Column sums recomputed without the oracle: numpy gather + torch fp64 softmax."""
+def independent_colsum(wl, causal=False):
+    """Column sums recomputed without the oracle: numpy gather + torch fp64 softmax
+    (causal=True masks key j for window query i when j > i)."""
     s = wl.spec
     G = s.hq // s.hkv
     k = wl.k.float().double().numpy()
@@ -61,6 +62,10 @@ def independent_colsum(wl):
             for g in range(s.hkv):
                 kw = torch.from_numpy(k[li, blk, g, slot, :])               # [W][D]
                 qg = q[si, li, g * G:(g + 1) * G].reshape(-1, s.d)           # [G*W][D]
-                p = torch.softmax((qg @ kw.T) / np.sqrt(s.d), dim=-1)
+                lg = (qg @ kw.T) / np.sqrt(s.d)
+                if causal:
+                    i = torch.arange(G * s.W) % s.W
+                    lg = lg.masked_fill(torch.arange(s.W)[None, :] > i[:, None], float("-inf"))
+                p = torch.softmax(lg, dim=-1)
                 out[si, li, g] = p.sum(dim=0).numpy()
     return out
