@@ -216,6 +216,9 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+VARIANT_CODES = {"bidirectional": 0, "causal": 1, "token2chunk": 0, "top_r": 1, "fixed_chunk": 2}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -226,6 +229,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--n-seq", type=int, default=None, help="override the workload's sequence count")
+    ap.add_argument("--score-mode", default="bidirectional", choices=["bidirectional", "causal"],
+                    help="scoring variant (causal is the ablation without bidirectional attention)")
+    ap.add_argument("--select-mode", default="token2chunk", choices=["token2chunk", "top_r", "fixed_chunk"],
+                    help="selection variant (top_r and fixed_chunk are the ablations of Token2Chunk)")
+    ap.add_argument("--chunk", type=int, default=0, help="chunk length for --select-mode fixed_chunk")
     ap.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     ap.add_argument("--profile-kernel", choices=["score", "select", "compact"], default=None,
                     help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
@@ -258,7 +266,8 @@ def main():
     wl = synth.generate(spec, device=dev)
     torch.cuda.synchronize()
     c = kara.cache(wl.k, wl.v, spec.hq)
-    p = kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam)
+    p = kara.params(spec.W, spec.B, spec.K, spec.R, spec.lam, VARIANT_CODES[args.score_mode],
+                    VARIANT_CODES[args.select_mode], args.chunk)
     lengths_h = wl.lengths.cpu()
     nn, no, tn, to = kara.kara_plan(p, spec.block, lengths_h, wl.bt_stride)
     bt0 = wl.block_table.clone()
@@ -360,6 +369,7 @@ def main():
         "config": {"workload": f"{args.config}: {spec.n_seq} seq x {spec.layers} layers x {spec.hkv} KV heads "
                                f"= {nwin} windows, W {spec.W} (C {spec.C} + B {spec.B}), G {spec.G}, D {spec.d}, "
                                f"Top-K {spec.K}, R {spec.R}",
+                   "variant": {"score": args.score_mode, "select": args.select_mode, "chunk": args.chunk},
                    "l2": "inputs larger than L2 (Q windows and K/V pools are tens of GB per step)",
                    "step": "block table restored by a device copy, then kara_compress_batch",
                    "parallelism": f"dp{ws_} (independent batches per GPU)"},

@@ -14,10 +14,10 @@ class Compressor:
     """
 
     def __init__(self, k: torch.Tensor, v: torch.Tensor, num_q_heads: int, W: int, B: int, K: int, R: int,
-                 lam: float = 0.1):
+                 lam: float = 0.1, score_mode: int = 0, select_mode: int = 0, chunk: int = 0):
         self.k, self.v = k, v
         self.cache = kara.cache(k, v, num_q_heads)
-        self.params = kara.params(W, B, K, R, lam)
+        self.params = kara.params(W, B, K, R, lam, score_mode, select_mode, chunk)
         self.err = torch.zeros(1, dtype=torch.int32, device=k.device)
         self._ws = torch.empty(0, dtype=torch.uint8, device=k.device)
 

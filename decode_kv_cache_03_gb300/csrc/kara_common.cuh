@@ -34,6 +34,7 @@ struct Geo {
     const int32_t *bt;
     const uint16_t *q;
     int64_t nwin;         // n * layers * hkv
+    int32_t causal;       // score_mode == KARA_SCORE_CAUSAL
 };
 
 __device__ __forceinline__ void set_err(int32_t *err, int code)
@@ -67,7 +68,7 @@ cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kep
                            int64_t n_fresh, int32_t *err, cudaStream_t st);
 cudaError_t launch_commit(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int32_t *freed,
                           int32_t *new_len, int32_t *bt, const int32_t *err, cudaStream_t st);
-cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, const float *scores,
+cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, int mode, int chunk, const float *scores,
                           int32_t *cand, int32_t *kept, cudaStream_t st);
 size_t score_scratch_bytes(const Geo &g);
 cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);

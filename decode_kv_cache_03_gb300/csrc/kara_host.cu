@@ -25,6 +25,9 @@ kara_status check_params(const kara_params *p)
     if (p->K > kMaxK) return KARA_EUNSUPPORTED;
     if (p->R < 1 || p->R > C) return KARA_EINVAL;
     if (!(p->lambda == p->lambda)) return KARA_EINVAL;  // NaN
+    if (p->score_mode != KARA_SCORE_BIDIRECTIONAL && p->score_mode != KARA_SCORE_CAUSAL) return KARA_EINVAL;
+    if (p->select_mode < KARA_SELECT_TOKEN2CHUNK || p->select_mode > KARA_SELECT_FIXED_CHUNK) return KARA_EINVAL;
+    if (p->select_mode == KARA_SELECT_FIXED_CHUNK && (p->chunk < 1 || p->chunk > C)) return KARA_EINVAL;
     return KARA_OK;
 }
 
@@ -78,6 +81,7 @@ kara_status make_geo(const kara_cache *c, const kara_params *p, const kara_batch
     g->bt = b->block_table;
     g->q = static_cast<const uint16_t *>(b->q);
     g->nwin = (int64_t)b->n * c->num_layers * c->num_kv_heads;
+    g->causal = p->score_mode == KARA_SCORE_CAUSAL;
     return KARA_OK;
 }
 
@@ -205,8 +209,8 @@ kara_status kara_select(const kara_params *p, int64_t n_windows, const float *sc
     if (n_windows == 0) return KARA_OK;
     if (!scores || !kept) return KARA_EINVAL;
     if (n_windows > 0x7fffffffLL) return KARA_EUNSUPPORTED;
-    return cuda_status(launch_select(n_windows, p->W - p->B, p->K, p->R, p->lambda, scores, cand, kept,
-                                     (cudaStream_t)stream));
+    return cuda_status(launch_select(n_windows, p->W - p->B, p->K, p->R, p->lambda, p->select_mode, p->chunk,
+                                     scores, cand, kept, (cudaStream_t)stream));
 }
 
 kara_status kara_compact(const kara_cache *c, const kara_params *p, const kara_batch *b,
@@ -257,7 +261,8 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = launch_score(g, scores, at<void>(ws, w.scratch), err, s);
     if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess) e = launch_select(g.nwin, g.C, g.K, g.R, g.lambda, scores, cand, kept, s);
+    if (e == cudaSuccess) e = launch_select(g.nwin, g.C, g.K, g.R, g.lambda, p->select_mode, p->chunk, scores, cand,
+                                            kept, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) e = launch_compact(g, plan, kept, fresh, n_fresh, err, s);
     if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);

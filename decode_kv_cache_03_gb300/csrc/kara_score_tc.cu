@@ -225,9 +225,9 @@ __device__ __forceinline__ void merge_rows(uint32_t part_u32, int r0, int r_hi, 
 // and stores log2 sum 2^l2 over those keys (shifted by their maximum) at
 // lse_half[2 * r + hf].  NLD is a template parameter so that one strip's
 // loads, maxima and exponentials form a single branch-free block.
-template <int NLD>
+template <int NLD, bool CAUSAL>
 __device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta0, int row, int hf, int T, int GW,
-                                           float c2, float *lse_half)
+                                           float c2, float *lse_half, int W, int key0)
 {
     const int lane = threadIdx.x & 31;
     for (int t = 0; t < T; ++t) {
@@ -242,10 +242,22 @@ __device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+        if (CAUSAL) {
+            // query i = r mod W sees keys key0 + col <= i only: later columns become -inf
+            const int lim = (t * kStrip + row) % W - key0;
+            if (!__all_sync(0xffffffffu, lim >= NLD * 32 - 1)) {
+#pragma unroll
+                for (int k = 0; k < NLD; ++k)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (k * 32 + c > lim) v[k][c] = 0xff800000u;
+            }
+        }
         float m = max32(v[0]);
 #pragma unroll
         for (int k = 1; k < NLD; ++k) m = fmaxf(m, max32(v[k]));
-        const float mc = m * c2;
+        // (causal) a row whose keys here are all masked gives z = 0 and lse -inf
+        const float mc = (CAUSAL && m == -INFINITY) ? 0.f : m * c2;
         uint64_t acc[4] = {0, 0, 0, 0};
         const uint64_t c2p = pack2(c2, c2), nmp = pack2(-mc, -mc);
 #pragma unroll
@@ -258,7 +270,9 @@ __device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta
     }
 }
 
-template <int D>
+// CAUSAL: the scoring ablation without bidirectional attention (query i sees
+// keys j <= i); a template parameter so that the default path carries no mask code.
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
                     int32_t *err, int ncta, int T, int stages, float c2)
@@ -435,10 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass 1: per row, log2-sum-exp over this warp half's keys of the slice
         float *lse_half = reinterpret_cast<float *>(part);
         switch (nld) {
-        case 1: pass1_rows<1>(sh, err, tmem + lane_base + hf * 32, row, hf, T, GW, c2, lse_half); break;
-        case 2: pass1_rows<2>(sh, err, tmem + lane_base + hf * 64, row, hf, T, GW, c2, lse_half); break;
-        case 3: pass1_rows<3>(sh, err, tmem + lane_base + hf * 96, row, hf, T, GW, c2, lse_half); break;
-        default: pass1_rows<4>(sh, err, tmem + lane_base + hf * 128, row, hf, T, GW, c2, lse_half); break;
+        case 1: pass1_rows<1, CAUSAL>(sh, err, tmem + lane_base + hf * 32, row, hf, T, GW, c2, lse_half, g.W,
+                                  slice0 + hf * 32); break;
+        case 2: pass1_rows<2, CAUSAL>(sh, err, tmem + lane_base + hf * 64, row, hf, T, GW, c2, lse_half, g.W,
+                                  slice0 + hf * 64); break;
+        case 3: pass1_rows<3, CAUSAL>(sh, err, tmem + lane_base + hf * 96, row, hf, T, GW, c2, lse_half, g.W,
+                                  slice0 + hf * 96); break;
+        default: pass1_rows<4, CAUSAL>(sh, err, tmem + lane_base + hf * 128, row, hf, T, GW, c2, lse_half, g.W,
+                                 slice0 + hf * 128); break;
         }
         __syncwarp();
         cluster_arrive();
@@ -493,7 +511,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
-            if (mine) {
+            bool skip = false;
+            if (CAUSAL && mine) {
+                // key j adds the weights of queries i >= j only: column n of the
+                // strip is query i = (t*128 + n) mod W
+                const int j = slice0 + hf * 128 + row, i0 = (t * kStrip) % g.W;
+                const bool wraps = i0 + kStrip > g.W;
+                const bool all_in = !wraps && i0 >= j;
+                const bool all_out = !wraps && i0 + kStrip - 1 < j;
+                skip = __all_sync(0xffffffffu, all_out);
+                if (!skip && !__all_sync(0xffffffffu, all_in)) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            int i = i0 + k * 32 + c;
+                            if (i >= g.W) i -= g.W;
+                            if (i < j) v[k][c] = 0xff800000u;
+                        }
+                }
+            }
+            if (mine && !skip) {
                 const float *nl = nlse2 + t * kStrip;
                 uint64_t pacc[4] = {0, 0, 0, 0};
                 const uint64_t c2p = pack2(c2, c2);
@@ -551,7 +589,7 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-    auto kern = score_tc_kernel<D>;
+    auto kern = g.causal ? score_tc_kernel<D, true> : score_tc_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -135,19 +135,22 @@ __device__ void radix_take(const float *s, int lo, int hi, int need, Elig elig, 
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R, float lambda,
-                                                             const float *__restrict__ scores,
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R, float lambda, int mode,
+                                                             int chunk, const float *__restrict__ scores,
                                                              int32_t *cand_out, int32_t *kept_out)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ SelShared sh;
     const int64_t u = blockIdx.x;
+    const int nfc = mode == KARA_SELECT_FIXED_CHUNK ? (C + chunk - 1) / chunk : 0;  // fixed chunks
     float *s = reinterpret_cast<float *>(smem);
     int32_t *cand = reinterpret_cast<int32_t *>(s + C);
     float *cs = reinterpret_cast<float *>(cand + K);
     int32_t *corder = reinterpret_cast<int32_t *>(cs + K);
     int32_t *corder2 = corder + K;
-    uint8_t *cflag = reinterpret_cast<uint8_t *>(corder2 + K);
+    float *fmean = reinterpret_cast<float *>(corder2 + K);
+    int32_t *forder = reinterpret_cast<int32_t *>(fmean + nfc);
+    uint8_t *cflag = reinterpret_cast<uint8_t *>(forder + nfc);
     uint8_t *kflag = cflag + C;
     uint8_t *taken = kflag + C;
 
@@ -178,6 +181,50 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R
     }
     __syncthreads();
 
+    if (mode == KARA_SELECT_TOP_R) {
+        // Token-level Top-R: the R positions first in the score order.
+        radix_take(s, lo, hi, R, [](int) { return true; }, kflag, sh);
+    } else if (mode == KARA_SELECT_FIXED_CHUNK) {
+        // Fixed chunks [k*chunk, min(C, (k+1)*chunk)) scored by their mean (a
+        // float sum in index order, then one rounded division) ...
+        for (int t = tid; t < nfc; t += kSelThreads) {
+            const int a = t * chunk, b = min(C, a + chunk);
+            float sum = 0.f;
+            for (int j = a; j < b; ++j) sum = __fadd_rn(sum, s[j]);
+            fmean[t] = __fdiv_rn(sum, (float)(b - a));
+        }
+        __syncthreads();
+        // ... visited by (mean desc, start asc) ...
+        for (int t = tid; t < nfc; t += kSelThreads) {
+            const uint32_t c = okey(fmean[t]);
+            int r = 0;
+            for (int t2 = 0; t2 < nfc; ++t2) {
+                const uint32_t c2 = okey(fmean[t2]);
+                r += (c2 > c) || (c2 == c && t2 < t);
+            }
+            forder[r] = t;
+        }
+        __syncthreads();
+        // ... and kept whole while they fit the budget (first fit) ...
+        if (tid == 0) {
+            int count = 0;
+            for (int r = 0; r < nfc; ++r) {
+                const int a = forder[r] * chunk, b = min(C, a + chunk);
+                if (count + (b - a) <= R) {
+                    for (int j = a; j < b; ++j) kflag[j] = 1;
+                    count += b - a;
+                }
+            }
+            sh.count = count;
+        }
+        __syncthreads();
+        // ... then the budget is filled with other positions in score order.
+        if (sh.count < R) {
+            const int need = R - sh.count;
+            __syncthreads();
+            radix_take(s, lo, hi, need, [&](int j) { return !kflag[j]; }, kflag, sh);
+        }
+    } else {
     // 3. Chunk scores.
     const int nch = K - 1;
     for (int t = tid; t < nch; t += kSelThreads) {
@@ -272,6 +319,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R
         __syncthreads();
         radix_take(s, lo, hi, need, [&](int j) { return !cflag[j] && !kflag[j]; }, kflag, sh);
     }
+    }  // Token2Chunk
 
     // 9. Outputs.
     if (cand_out)
@@ -287,17 +335,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int C, int K, int R
 
 }  // namespace
 
-size_t select_smem_bytes(int C, int K)
+size_t select_smem_bytes(int C, int K, int mode, int chunk)
 {
-    return (size_t)C * 4 + (size_t)K * 4 * 4 + (size_t)C * 2 + (size_t)K;
+    const size_t nfc = mode == KARA_SELECT_FIXED_CHUNK ? (size_t)(C + chunk - 1) / chunk : 0;
+    return (size_t)C * 4 + (size_t)K * 4 * 4 + nfc * 8 + (size_t)C * 2 + (size_t)K;
 }
 
-cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, const float *scores,
-                          int32_t *cand, int32_t *kept, cudaStream_t st)
+cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, int mode, int chunk,
+                          const float *scores, int32_t *cand, int32_t *kept, cudaStream_t st)
 {
     if (nwin == 0) return cudaSuccess;
-    const size_t smem = select_smem_bytes(C, K);
-    select_kernel<<<(unsigned)nwin, kSelThreads, smem, st>>>(C, K, R, lambda, scores, cand, kept);
+    const size_t smem = select_smem_bytes(C, K, mode, chunk);
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    select_kernel<<<(unsigned)nwin, kSelThreads, smem, st>>>(C, K, R, lambda, mode, chunk, scores, cand, kept);
     return cudaGetLastError();
 }
 

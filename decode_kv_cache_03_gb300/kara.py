@@ -28,7 +28,13 @@ class KaraError(RuntimeError):
 
 class Params(ctypes.Structure):
     _fields_ = [("W", ctypes.c_int32), ("B", ctypes.c_int32), ("K", ctypes.c_int32),
-                ("R", ctypes.c_int32), ("lam", ctypes.c_float)]
+                ("R", ctypes.c_int32), ("lam", ctypes.c_float), ("score_mode", ctypes.c_int32),
+                ("select_mode", ctypes.c_int32), ("chunk", ctypes.c_int32)]
+
+
+# kara_score_mode / kara_select_mode
+SCORE_BIDIRECTIONAL, SCORE_CAUSAL = 0, 1
+SELECT_TOKEN2CHUNK, SELECT_TOP_R, SELECT_FIXED_CHUNK = 0, 1, 2
 
 
 class Cache(ctypes.Structure):
@@ -99,8 +105,8 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def params(W, B, K, R, lam) -> Params:
-    return Params(int(W), int(B), int(K), int(R), float(lam))
+def params(W, B, K, R, lam, score_mode=SCORE_BIDIRECTIONAL, select_mode=SELECT_TOKEN2CHUNK, chunk=0) -> Params:
+    return Params(int(W), int(B), int(K), int(R), float(lam), int(score_mode), int(select_mode), int(chunk))
 
 
 def cache(k: torch.Tensor, v: torch.Tensor, num_q_heads: int) -> Cache:

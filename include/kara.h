@@ -61,13 +61,35 @@ typedef enum {
     KARA_EWORKSPACE = -8     /* workspace missing or smaller than kara_workspace_size */
 } kara_status;
 
-/* Method parameters.  R is an explicit token count per window. */
+/*
+ * Scoring and selection variants.  Mode 0 of each is the method as the pages
+ * describe it.  The others are the ablations the summary's "Experimental
+ * Results" (ablation studies) reports -- scores without bidirectional
+ * attention, selection without Token2Chunk -- and the fixed-size chunks with
+ * rigid boundaries its "Problem Statement" (item 2) sets Token2Chunk against.
+ */
+typedef enum {
+    KARA_SCORE_BIDIRECTIONAL = 0,  /* every window query attends to all W window keys */
+    KARA_SCORE_CAUSAL = 1          /* window query i attends to window keys j <= i only */
+} kara_score_mode;
+
+typedef enum {
+    KARA_SELECT_TOKEN2CHUNK = 0,   /* Top-K candidates expanded into chunks (kara_select) */
+    KARA_SELECT_TOP_R = 1,         /* the R positions first in score order, no chunks */
+    KARA_SELECT_FIXED_CHUNK = 2    /* chunks [k*chunk, (k+1)*chunk) ranked by mean score */
+} kara_select_mode;
+
+/* Method parameters.  R is an explicit token count per window.  A zeroed
+ * score_mode / select_mode / chunk gives the method as described. */
 typedef struct {
     int32_t W;       /* window: the W most recent tokens of a sequence */
     int32_t B;       /* protected buffer at the end of the window, 0 <= B < W */
     int32_t K;       /* Top-K candidates per window */
     int32_t R;       /* tokens each window keeps out of its C compressible ones */
     float lambda;    /* chunk length penalty in (s_a + s_b) / (1 + lambda * len) */
+    int32_t score_mode;   /* kara_score_mode */
+    int32_t select_mode;  /* kara_select_mode */
+    int32_t chunk;        /* chunk length for KARA_SELECT_FIXED_CHUNK, 1 <= chunk <= C; else ignored */
 } kara_params;
 
 /* Paged K/V pools.  Element (l, blk, g, slot, d) of a pool lives at
@@ -121,6 +143,8 @@ size_t kara_workspace_size(const kara_cache *c, const kara_params *p, int32_t n)
  * every query head h of the group and every window query i < W:
  *     p[h,i,j] = softmax_j( <q_{h,i}, k_j> / sqrt(D) ),  j < W  (no causal mask)
  * and  scores[u][j] = sum_h sum_i p[h,i,j]  for the compressible keys j < C.
+ * With score_mode KARA_SCORE_CAUSAL (an ablation) the softmax of query i runs
+ * over the keys j <= i only and p[h,i,j] = 0 for j > i.
  * k_j is the key at logical position ws + j, read through the block table.
  * Logits accumulate in fp32 from bf16; the softmax and sums are fp32.
  * scores: device float [n][num_layers][num_kv_heads][C].
@@ -134,6 +158,12 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
 
 /*
  * Top-K and Token2Chunk (summary section 1 "Selection"; section 2 "Process").
+ * (select_mode KARA_SELECT_TOP_R and KARA_SELECT_FIXED_CHUNK replace the
+ * chunk step, keeping cand as below: kept is the R first positions in the
+ * score order; or chunks [k*chunk, min(C,(k+1)*chunk)) scored by their mean
+ * -- a float sum in index order divided by the length -- visited by (mean
+ * desc, start asc), kept whole when they fit R, then filled to exactly R with
+ * other positions in score order.)
  * For each of n_windows windows with C fp32 scores:
  *   cand: the K positions first in the order (score desc, index asc), sorted
  *         by index.

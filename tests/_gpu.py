@@ -22,12 +22,12 @@ def to_device(wl: synth.Workload) -> synth.Workload:
                           wl.block_table.to(d).contiguous(), wl.fresh.to(d), wl.prefix_pool, wl.fresh_base)
 
 
-def run_compress(wl_dev: synth.Workload, n_fresh=None):
+def run_compress(wl_dev: synth.Workload, n_fresh=None, score_mode=0, select_mode=0, chunk=0):
     """kara_compress_batch on device data; returns host copies of every output."""
     kara = lib()
     s = wl_dev.spec
     c = kara.cache(wl_dev.k, wl_dev.v, s.hq)
-    p = kara.params(s.W, s.B, s.K, s.R, s.lam)
+    p = kara.params(s.W, s.B, s.K, s.R, s.lam, score_mode, select_mode, chunk)
     bt = wl_dev.block_table.clone()
     b = kara.batch(wl_dev.lengths, bt, wl_dev.q)
     nn, no, tn, to = kara.kara_plan(p, s.block, wl_dev.lengths.cpu(), wl_dev.bt_stride)

@@ -94,6 +94,10 @@ def test_argument_checks_happen_before_any_device_work(kara):
         (fake_cache(kara), kara.params(64, 16, 8, 49, 0.1), kara.EINVAL),
         (fake_cache(kara), kara.params(64, 16, 8, 0, 0.1), kara.EINVAL),
         (fake_cache(kara), kara.params(4096, 16, 8, 16, 0.1), kara.EUNSUPPORTED),
+        (fake_cache(kara), kara.params(64, 16, 8, 16, 0.1, score_mode=2), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 8, 16, 0.1, select_mode=3), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 8, 16, 0.1, select_mode=2, chunk=0), kara.EINVAL),
+        (fake_cache(kara), kara.params(64, 16, 8, 16, 0.1, select_mode=2, chunk=49), kara.EINVAL),
     ]
     for c, pp, want in cases:
         st = kara._lib.kara_compress_batch(ctypes.byref(c), ctypes.byref(pp), ctypes.byref(b), ws, 4, ws, ws,
