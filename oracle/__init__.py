@@ -64,6 +64,7 @@ def lib():
                                   ctypes.c_int, ctypes.c_int, P, P]
         _lib.kro_compact.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, ctypes.c_int64, P, P]
         _lib.kro_max_threads.restype = ctypes.c_int
+        _lib.kro_decode_attention.argtypes = [ctypes.POINTER(Shape), ctypes.c_int, P, P, P, P, P, P, ctypes.c_int]
     return _lib
 
 
@@ -159,6 +160,22 @@ def select_batch(scores_arr, K: int, R: int, lam: float, nthreads=None):
     if st != OK:
         raise ValueError(f"oracle select failed: status {st}")
     return cand, kept
+
+
+def decode_attention(shape: Shape, layer: int, q, kpool, vpool, block_table, lengths, nthreads=None):
+    """Decode attention of one query per (sequence, query head) over the paged
+    cache of one layer: float [n_seq][hq][d]."""
+    qa = _np(q, np.uint16)
+    ka = _np(kpool, np.uint16)
+    va = _np(vpool, np.uint16)
+    bt = _np(block_table, np.int32)
+    ln = _np(lengths, np.int32)
+    out = np.zeros((shape.n_seq, shape.hq, shape.d), np.float32)
+    st = lib().kro_decode_attention(ctypes.byref(shape), int(layer), _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt),
+                                    _ptr(ln), _ptr(out), int(nthreads or max_threads()))
+    if st != OK:
+        raise ValueError(f"oracle decode attention failed: status {st}")
+    return out
 
 
 SELECT_TOKEN2CHUNK, SELECT_TOP_R, SELECT_FIXED_CHUNK = 0, 1, 2

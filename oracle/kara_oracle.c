@@ -14,8 +14,10 @@
  * Scoring", "2. Token2Chunk Module" and "3. KvLLM Framework and Periodic
  * Compression"; the ablation variants (causal scores, token-level Top-R,
  * fixed-size chunks) follow its "Experimental Results" (ablation studies) and
- * "Problem Statement" (item 2).  The pages give no formula; every reading
- * taken where they are silent is named at the function that takes it.
+ * "Problem Statement" (item 2); decode attention over the compacted cache
+ * follows section "3. KvLLM Framework and Periodic Compression".  The pages
+ * give no formula; every reading taken where they are silent is named at the
+ * function that takes it.
  *
  * Notation, per window u = (sequence s, layer l, KV head g):
  *   L  cached length, W window, ws = L - W window start (logical position),
@@ -182,6 +184,66 @@ int kro_scores_causal(const kro_shape *sh, const uint16_t *q, const uint16_t *kp
                       const int32_t *len, float *scores, double *colsum, int nthreads)
 {
     return scores_impl(sh, 1, q, kpool, bt, len, scores, colsum, nthreads);
+}
+
+/*
+ * Decode attention over the paged cache: the reader of the tables the step
+ * rewrites (summary section 3, "KvLLM Framework and Periodic Compression":
+ * Kara adapted to PagedAttention, and the freed memory serves more decoding
+ * sequences).  One decode query per sequence and query head h (KV head
+ * g = h / G) attends to every cached key x in [0, L) of one layer:
+ *     l[x] = sigma * <q_h, k_x>,   o_h = sum_x exp(l[x] - max l) v_x / sum_x exp(l[x] - max l)
+ * in double from the exact bf16 values, each output element rounded once to
+ * float.  Reading: plain decode attention with no mask inside the cache (the
+ * pages name PagedAttention and print no kernel); sigma = 1/sqrt(D) as above.
+ * q: bf16 bits [n_seq][hq][d]; out: float [n_seq][hq][d].
+ */
+int kro_decode_attention(const kro_shape *sh, int layer, const uint16_t *q, const uint16_t *kpool,
+                         const uint16_t *vpool, const int32_t *bt, const int32_t *len, float *out, int nthreads)
+{
+    const int D = sh->d, G = sh->hq / sh->hkv;
+    const double sigma = 1.0 / sqrt((double)D);
+    int status = KRO_OK;
+    if (layer < 0 || layer >= sh->layers || sh->hq % sh->hkv != 0) return KRO_EINVAL;
+    for (int s = 0; s < sh->n_seq; ++s)
+        if (len[s] < 1 || (len[s] + sh->block - 1) / sh->block > sh->bt_stride) return KRO_EINVAL;
+    if (nthreads < 1) nthreads = 1;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t sh_idx = 0; sh_idx < (int64_t)sh->n_seq * sh->hq; ++sh_idx) {
+        const int s = (int)(sh_idx / sh->hq), h = (int)(sh_idx % sh->hq), g = h / G;
+        const int64_t L = len[s];
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        double *lg = (double *)malloc(sizeof(double) * (size_t)L);
+        double *acc = (double *)calloc((size_t)D, sizeof(double));
+        const uint16_t *qrow = q + ((int64_t)s * sh->hq + h) * D;
+        for (int e = 0; e < D; ++e) qd[e] = bf16_to_double(qrow[e]);
+        int bad = 0;
+        double m = -INFINITY;
+        for (int64_t x = 0; x < L && !bad; ++x) {
+            const uint16_t *kr = pool_row(sh, kpool, bt, s, layer, g, x);
+            if (!kr) { bad = 1; break; }
+            double dot = 0.0;
+            for (int e = 0; e < D; ++e) dot += qd[e] * bf16_to_double(kr[e]);
+            lg[x] = sigma * dot;
+            if (lg[x] > m) m = lg[x];
+        }
+        double Z = 0.0;
+        for (int64_t x = 0; x < L && !bad; ++x) {
+            const uint16_t *vr = pool_row(sh, vpool, bt, s, layer, g, x);
+            const double w = exp(lg[x] - m);
+            Z += w;
+            for (int e = 0; e < D; ++e) acc[e] += w * bf16_to_double(vr[e]);
+        }
+        if (bad) {
+#pragma omp atomic write
+            status = KRO_EBADBLOCK;
+        } else {
+            for (int e = 0; e < D; ++e) out[sh_idx * D + e] = (float)(acc[e] / Z);
+        }
+        free(qd); free(lg); free(acc);
+    }
+    return status;
 }
 
 /* ---- selection ---------------------------------------------------------- */

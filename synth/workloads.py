@@ -298,3 +298,9 @@ def host_subset(wl: Workload, seqs: list[int]) -> Workload:
 def bf16_bits(t: torch.Tensor) -> torch.Tensor:
     """Raw 16-bit patterns of a bf16 tensor (as int16)."""
     return t.contiguous().view(torch.int16)
+
+
+def decode_queries(spec: Spec, seed: int = 0, device="cpu") -> torch.Tensor:
+    """One decode query per sequence and query head: bf16 [n_seq][hq][d], ~N(0,1)."""
+    g = _gen(10_000 + seed, device)
+    return torch.randn(spec.n_seq, spec.hq, spec.d, generator=g, device=device).to(torch.bfloat16)
