@@ -239,6 +239,8 @@ def main():
                     help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
     ap.add_argument("--sweep", action="store_true",
                     help="periodic-policy sweep on the Qwen3-4B shape: one JSON line per compression event")
+    ap.add_argument("--decode", action="store_true",
+                    help="decode attention over the paged cache (one layer of the workload): one JSON line")
     ap.add_argument("--sweep-batches", default="1,8,32,128,256")
     ap.add_argument("--sweep-windows", default="128,256,512,1024,2048")
     args = ap.parse_args()
@@ -257,6 +259,9 @@ def main():
     dev = torch.device("cuda", local)
     if args.sweep:
         run_sweep(args, dev)
+        return
+    if args.decode:
+        run_decode(args, dev, kara)
         return
     spec = synth.SPECS[args.config].with_(seed=synth.SPECS[args.config].seed + 97 * rank)
     if args.n_seq:
@@ -478,6 +483,50 @@ def run_sweep(args, dev):
                                                 roofline_frac=t_roof / (ms * 1e-3), peaks=src)}), flush=True)
             del wl, q, comp
             torch.cuda.empty_cache()
+
+
+def run_decode(args, dev, kara):
+    """Decode attention of one query per (sequence, query head) over one layer of
+    the workload's paged cache, every block stored once (no aliased prefix), so
+    the K/V bytes really come from HBM.  Bound: HBM; bytes per launch =
+    sum_s L_s * Hkv * D * 2 (K and V) * 2 B, plus queries and outputs."""
+    spec = synth.SPECS[args.config].with_(layers=1)
+    if args.n_seq:
+        spec = spec.with_(n_seq=args.n_seq)
+    wl = synth.generate(spec, device=dev, alias_prefix=False, with_q=False)
+    q = synth.decode_queries(spec, 0, device=dev)
+    c = kara.cache(wl.k, wl.v, spec.hq)
+    n, bt_stride = wl.block_table.shape
+    ws = torch.empty(kara.kara_decode_workspace_size(c, n, bt_stride), dtype=torch.uint8, device=dev)
+    out = torch.empty(n, spec.hq, spec.d, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        kara.kara_decode_attention(c, 0, wl.lengths, wl.block_table, q, out, ws, err)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            kara.kara_decode_attention(c, 0, wl.lengths, wl.block_table, q, out, ws, err)
+        e1.record()
+        torch.cuda.synchronize()
+    status = kara.kara_get_error(err)
+    if status != 0:
+        raise SystemExit(f"decode attention reported {kara.status_string(status)}")
+    ms = e0.elapsed_time(e1) / args.steps
+    kv_bytes = int(wl.lengths.to(torch.int64).sum()) * spec.hkv * spec.d * 2 * 2
+    io_bytes = q.numel() * 2 + out.numel() * 4 + wl.block_table.numel() * 4
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    pk = peaks()[0]
+    line = {"metric": "decode attention over the paged cache (HBM GB/s)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16 in, f32 math", "data": "synthetic",
+            "config": {"workload": f"{args.config}, one layer: {n} sequences x {spec.hq} query / {spec.hkv} KV heads, "
+                                   f"D {spec.d}, lengths {spec.len_lo}..{spec.len_hi}, {kv_bytes / 1e9:.2f} GB of K/V",
+                       "l2": "K/V larger than L2, every block distinct"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk, "unit": "GB/s", "frac": gbs / pk},
+            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
 
 
 def launches_per_step():

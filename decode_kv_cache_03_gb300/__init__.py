@@ -25,6 +25,8 @@ _LAZY = {
     "kara_compact": ("kara", "kara_compact"),
     "kara_compress_batch": ("kara", "kara_compress_batch"),
     "kara_get_error": ("kara", "kara_get_error"),
+    "kara_decode_attention": ("kara", "kara_decode_attention"),
+    "kara_decode_workspace_size": ("kara", "kara_decode_workspace_size"),
 }
 
 __all__ = sorted(_LAZY)

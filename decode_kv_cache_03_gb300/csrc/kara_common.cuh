@@ -71,6 +71,10 @@ cudaError_t launch_commit(const Geo &g, const SeqPlan *plan, const int32_t *fres
 cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, int mode, int chunk, const float *scores,
                           int32_t *cand, int32_t *kept, cudaStream_t st);
 size_t score_scratch_bytes(const Geo &g);
+cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const int32_t *len, const int32_t *bt,
+                          int32_t bt_stride, const void *q, float *out, void *ws, int32_t *err, cudaStream_t st);
+size_t decode_workspace_bytes(const kara_cache *c, int32_t n, int32_t bt_stride);
+int decode_max_splits(int32_t bt_stride, int32_t block_size);
 cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
 
 }  // namespace kara

@@ -200,6 +200,29 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
     return cuda_status(launch_score(g, scores, ws, err, (cudaStream_t)stream));
 }
 
+size_t kara_decode_workspace_size(const kara_cache *c, int32_t n, int32_t bt_stride)
+{
+    if (check_cache(c) != KARA_OK || n < 0 || bt_stride < 1) return 0;
+    return decode_workspace_bytes(c, n, bt_stride);
+}
+
+kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n, const int32_t *len,
+                                  const int32_t *block_table, int32_t bt_stride, const void *q, float *out,
+                                  void *ws, size_t ws_bytes, int32_t *err, kara_stream_t stream)
+{
+    kara_status st = check_cache(c);
+    if (st != KARA_OK) return st;
+    if (layer < 0 || layer >= c->num_layers || n < 0 || bt_stride < 1) return KARA_EINVAL;
+    if (n == 0) return KARA_OK;
+    if (!len || !block_table || !q || !out || !err) return KARA_EINVAL;
+    if (!aligned16(q)) return KARA_EINVAL;
+    if (n > 65535 || c->num_kv_heads > 65535 || c->num_q_heads > 65535) return KARA_EUNSUPPORTED;
+    if ((int64_t)bt_stride * c->block_size > 0x7fffffffLL) return KARA_EUNSUPPORTED;
+    if (!ws || ws_bytes < decode_workspace_bytes(c, n, bt_stride)) return KARA_EWORKSPACE;
+    return cuda_status(launch_decode(c, layer, n, len, block_table, bt_stride, q, out, ws, err,
+                                     (cudaStream_t)stream));
+}
+
 kara_status kara_select(const kara_params *p, int64_t n_windows, const float *scores, int32_t *cand,
                         int32_t *kept, kara_stream_t stream)
 {

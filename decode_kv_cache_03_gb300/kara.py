@@ -68,6 +68,8 @@ def _load():
         "kara_compress_batch": ([PC, PP, PB, P, I64, P, P, P, P, P, P, SZ, P, P, P], ctypes.c_int),
         "kara_get_error": ([P, P], ctypes.c_int),
         "kara_compact_static": ([PC, PP, PB, P, P, I64, P, P, P, P], ctypes.c_int),
+        "kara_decode_workspace_size": ([PC, I32, I32], SZ),
+        "kara_decode_attention": ([PC, I32, I32, P, P, I32, P, P, P, SZ, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -78,7 +80,8 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("kara_status_string", "kara_version", "kara_plan", "kara_workspace_size", "kara_score",
-            "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error", "kara_compact_static")
+            "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error", "kara_compact_static",
+            "kara_decode_workspace_size", "kara_decode_attention")
 STATIC_MAX_SEQS = 8192     # KARA_STATIC_MAX_SEQS
 
 
@@ -145,6 +148,23 @@ def kara_score(c: Cache, p: Params, b: Batch, scores: torch.Tensor, ws: torch.Te
                stream=None):
     _check(_lib.kara_score(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(scores), _ptr(ws),
                            ws.numel() * ws.element_size(), _ptr(err), _stream(stream)), "kara_score")
+
+
+def kara_decode_workspace_size(c: Cache, n: int, bt_stride: int) -> int:
+    return int(_lib.kara_decode_workspace_size(ctypes.byref(c), int(n), int(bt_stride)))
+
+
+def kara_decode_attention(c: Cache, layer: int, lengths: torch.Tensor, block_table: torch.Tensor,
+                          q: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, err: torch.Tensor, stream=None):
+    """Decode attention of q [n][num_q_heads][head_dim] (bf16) over layer `layer`
+    of the paged cache, read through block_table [n][bt_stride]; out is float."""
+    assert lengths.dtype == torch.int32 and block_table.dtype == torch.int32 and block_table.is_contiguous()
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and out.dtype == torch.float32
+    n, bt_stride = block_table.shape
+    _check(_lib.kara_decode_attention(ctypes.byref(c), int(layer), int(n), _ptr(lengths), _ptr(block_table),
+                                      int(bt_stride), _ptr(q), _ptr(out), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(err), _stream(stream)),
+           "kara_decode_attention")
 
 
 def kara_select(p: Params, n_windows: int, scores: torch.Tensor, cand, kept: torch.Tensor, stream=None):

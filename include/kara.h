@@ -157,6 +157,29 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
                        kara_stream_t stream);
 
 /*
+ * Decode attention over the paged cache (summary section 3: Kara adapted to
+ * PagedAttention; the blocks a compression frees serve more decoding
+ * sequences).  It reads K and V through the same block table that
+ * kara_compact rewrites, so it is the consumer of the step's output.  For
+ * each of n sequences and each query head h (KV head g = h / G):
+ *     out[s][h] = sum_{x < len[s]} softmax_x(<q[s][h], k_x> / sqrt(D)) v_x
+ * over the keys of layer `layer`, k_x and v_x at logical position x read
+ * through block_table.  fp32 logits, softmax and sums; fp32 output.
+ * len [n] (device); block_table [n][bt_stride] (device); q: bf16
+ * [n][num_q_heads][head_dim] (device, 16-byte aligned); out: float
+ * [n][num_q_heads][head_dim] (device).
+ * ws/ws_bytes: at least kara_decode_workspace_size(c, n, bt_stride) bytes.
+ * err: device int32; a length outside [1, bt_stride*block_size] records
+ * KARA_EINVAL and that sequence's output is 0; a block id outside the pool
+ * records KARA_EBADBLOCK (the row is read as zeros, never from outside the pool).
+ * Supported: the kara_cache shapes above; n <= 65535.
+ */
+size_t kara_decode_workspace_size(const kara_cache *c, int32_t n, int32_t bt_stride);
+kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n, const int32_t *len,
+                                  const int32_t *block_table, int32_t bt_stride, const void *q, float *out,
+                                  void *ws, size_t ws_bytes, int32_t *err, kara_stream_t stream);
+
+/*
  * Top-K and Token2Chunk (summary section 1 "Selection"; section 2 "Process").
  * (select_mode KARA_SELECT_TOP_R and KARA_SELECT_FIXED_CHUNK replace the
  * chunk step, keeping cand as below: kept is the R first positions in the

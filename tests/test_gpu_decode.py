@@ -1,0 +1,91 @@
+"""GPU parity of decode attention over the paged cache against the oracle,
+including the cache a compression call has just rewritten.
+
+Tolerance: the logits are fp32 dot products of exact bf16 products (relative
+error about D * 2^-24) and the weighted sums are fp32 over at most a few
+thousand rows, so for unit-scale V the output is within 1e-4 absolute of the
+fp64 result; the test allows 2e-4 absolute plus 1e-3 relative."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _cases import random_spec
+from _gpu import lib, run_compress, to_device
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-4, 1e-3
+
+
+def run_decode(kara, k, v, hq, layer, lengths, bt, q):
+    c = kara.cache(k, v, hq)
+    n, bt_stride = bt.shape
+    ws = torch.empty(kara.kara_decode_workspace_size(c, n, bt_stride), dtype=torch.uint8, device="cuda")
+    out = torch.full((n, hq, k.shape[-1]), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_decode_attention(c, layer, lengths, bt, q, out, ws, err)
+    return out.cpu().numpy(), kara.kara_get_error(err)
+
+
+@pytest.mark.parametrize("G,D,len_lo,len_hi", [
+    (1, 64, 1, 40), (2, 64, 100, 700), (4, 128, 20, 600), (5, 128, 1500, 2100), (8, 128, 500, 1100),
+    (3, 64, 1023, 1026), (6, 128, 2047, 2049), (7, 128, 1, 1)])
+def test_decode_matches_oracle(G, D, len_lo, len_hi):
+    """Lengths below, at and across the 1024-key split, one cached token, and G = 1..8."""
+    kara = lib()
+    spec = random_spec(500 + G * D + len_lo, G=G, hkv=2, W=64, B=16, D=D, n_seq=4, layers=2,
+                       len_lo=max(len_lo, 64), len_hi=max(len_hi, 64))
+    wl = synth.generate(spec)
+    if len_hi < 64:   # shorter than any window: keep the first len tokens of each table
+        gen = torch.Generator().manual_seed(len_hi)
+        wl.lengths.copy_(torch.randint(len_lo, len_hi + 1, (spec.n_seq,), generator=gen, dtype=torch.int32))
+    q = synth.decode_queries(spec, G)
+    d = to_device(wl)
+    for layer in (0, 1):
+        got, st = run_decode(kara, d.k, d.v, wl.spec.hq, layer, d.lengths, d.block_table, q.cuda())
+        assert st == 0
+        ref = oracle.decode_attention(oracle.shape_of(wl), layer, q, wl.k, wl.v, wl.block_table, wl.lengths)
+        np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
+
+
+def test_decode_reads_the_table_compression_rewrote():
+    """Compress, then decode over the rewritten table and shorter lengths: the
+    same result as the oracle decoding the oracle's compacted cache."""
+    kara = lib()
+    spec = random_spec(510, G=4, hkv=2, W=256, B=32, D=128, n_seq=3, layers=2, len_lo=600, len_hi=1500, K=16,
+                       R=60, plant="bernoulli")
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    out = run_compress(d)
+    assert out["status"] == 0
+    kh = wl.k.view(torch.int16).numpy().view(np.uint16)
+    vh = wl.v.view(torch.int16).numpy().view(np.uint16)
+    st, k2, v2, bt2, _, nl2 = oracle.compact(oracle.shape_of(wl), kh, vh, wl.block_table, wl.lengths, out["kept"],
+                                             wl.fresh)
+    assert st == oracle.OK and np.array_equal(out["bt"], bt2) and np.array_equal(out["new_len"], nl2)
+    q = synth.decode_queries(spec, 9)
+    for layer in (0, 1):
+        got, st = run_decode(kara, d.k, d.v, spec.hq, layer, torch.from_numpy(nl2).cuda(),
+                             torch.from_numpy(bt2).cuda().contiguous(), q.cuda())
+        assert st == 0
+        ref = oracle.decode_attention(oracle.shape_of(wl), layer, q, torch.from_numpy(k2.view(np.int16)),
+                                      torch.from_numpy(v2.view(np.int16)), bt2, nl2)
+        np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
+
+
+def test_decode_reports_bad_lengths_and_blocks():
+    kara = lib()
+    spec = random_spec(511, G=2, hkv=2, W=64, B=16, D=64, n_seq=3, layers=1, len_lo=100, len_hi=200)
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    q = synth.decode_queries(spec).cuda()
+    ln = d.lengths.clone()
+    ln[1] = 0
+    got, st = run_decode(kara, d.k, d.v, spec.hq, 0, ln, d.block_table, q)
+    assert st == kara.EINVAL and np.all(got[1] == 0) and np.all(np.isfinite(got))
+    bt = d.block_table.clone()
+    bt[2, 1] = wl.num_blocks + 5      # outside the pool: reported, never dereferenced
+    got, st = run_decode(kara, d.k, d.v, spec.hq, 0, d.lengths, bt, q)
+    assert st == kara.EBADBLOCK
