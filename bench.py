@@ -239,6 +239,8 @@ def main():
                     help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
     ap.add_argument("--sweep", action="store_true",
                     help="periodic-policy sweep on the Qwen3-4B shape: one JSON line per compression event")
+    ap.add_argument("--serve-sim", action="store_true",
+                    help="admission scheduler over a fixed block pool, with and without periodic compression")
     ap.add_argument("--decode", action="store_true",
                     help="decode attention over the paged cache (one layer of the workload): one JSON line")
     ap.add_argument("--sweep-batches", default="1,8,32,128,256")
@@ -262,6 +264,9 @@ def main():
         return
     if args.decode:
         run_decode(args, dev, kara)
+        return
+    if args.serve_sim:
+        run_serve_sim(args, dev)
         return
     spec = synth.SPECS[args.config].with_(seed=synth.SPECS[args.config].seed + 97 * rank)
     if args.n_seq:
@@ -527,6 +532,60 @@ def run_decode(args, dev, kara):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk, "unit": "GB/s", "frac": gbs / pk},
             "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
+
+
+def run_serve_sim(args, dev):
+    """The concurrency argument of the pages (summary, "Problem Statement" item 1
+    and section 3) on synthetic decoding: requests share a fixed pool of KV
+    blocks under the admission scheduler, once without compression and once
+    with the periodic policy compressing through kara_compress_batch.  Prints
+    one JSON line per run: mean running sequences, tokens decoded, requests
+    finished and the device time of the compression calls."""
+    from decode_kv_cache_03_gb300 import Compressor
+    from decode_kv_cache_03_gb300.periodic import AdmissionScheduler, BlockPool, PeriodicSchedule
+    base = synth.sweep_spec(1, 512)
+    layers, total, steps, nreq = 4, 16384, 3000, 256
+    k = torch.empty(layers, total, base.hkv, base.block, base.d, dtype=torch.bfloat16, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(1)
+    for l in range(layers):
+        k[l] = torch.randn(total, base.hkv, base.block, base.d, generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn_like(k)
+    rng = torch.Generator().manual_seed(2)
+    reqs = [(int(torch.randint(512, 1025, (1,), generator=rng)), int(torch.randint(2048, 6145, (1,), generator=rng)))
+            for _ in range(nreq)]
+
+    def q_window(n):
+        return torch.randn(n, layers, base.hq, base.W, base.d, generator=gen, device=dev).to(torch.bfloat16)
+
+    for compress in (False, True):
+        comp = Compressor(k, v, base.hq, base.W, base.B, base.K, base.R, base.lam)
+        sched = AdmissionScheduler(BlockPool(range(total)), reqs, base.block, bt_stride=(1024 + 6144) // 16 + 1)
+        schedule = PeriodicSchedule(128, 0.5, base.W, seed=3)
+        running, ev_ms, freed = [], [], 0
+        t0 = time.perf_counter()
+        for step in range(1, steps + 1):
+            sched.admit()
+            sched.step()
+            running.append(len(sched.running))
+            if compress and schedule.due(step):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                freed += sched.compress(comp, schedule, q_window)
+                e1.record()
+                torch.cuda.synchronize()
+                ev_ms.append(e0.elapsed_time(e1))
+        wall = time.perf_counter() - t0
+        line = {"metric": "serving simulation: tokens decoded in a fixed block pool", "value": sched.tokens,
+                "unit": "tokens", "steps": steps, "compression": compress,
+                "mean_running": statistics.mean(running), "max_running": max(running),
+                "finished": len(sched.finished), "compress_events": len(ev_ms), "blocks_freed": freed,
+                "compress_ms_mean": statistics.mean(ev_ms) if ev_ms else 0.0, "host_seconds": wall,
+                "config": {"pool_blocks": total, "block": base.block, "layers": layers,
+                           "heads": f"{base.hq}/{base.hkv}", "D": base.d, "W": base.W, "B": base.B, "K": base.K,
+                           "R": base.R, "requests": nreq, "prompt": "512..1024", "generate": "2048..6144",
+                           "policy": "every 128 steps, half of the eligible sequences"},
+                "data": "synthetic"}
+        print(json.dumps(line), flush=True)
 
 
 def launches_per_step():

@@ -103,3 +103,109 @@ def compress_selected(comp, seqs, lengths_host, table_host, q_window, pool: Bloc
     fr = freed[:to].cpu().tolist()
     pool.give(fr)
     return fr, status
+
+
+class AdmissionScheduler:
+    """Decoding sequences sharing a fixed pool of KV blocks, with optional
+    periodic compression (summary, "Problem Statement" item 1 and section 3:
+    memory bounds how many sequences decode at once, and the periodic policy
+    frees blocks so more of them can).
+
+    A request (prompt tokens, tokens to generate) waits in arrival order and is
+    admitted when the pool can hold the blocks it will need to finish,
+    counted from its current length without further compression, on top of
+    what the running sequences may still need.  So no sequence ever waits for
+    a block and the pool never deadlocks.  Each decode step appends one token to
+    every running sequence; a sequence finishes once it has generated its
+    tokens and returns its blocks.  With a compressor, every period of the
+    schedule the chosen sequences go through compress_selected: their cached
+    length drops by C - R, their freed blocks return to the pool, and the
+    blocks they may still need shrink, so more requests are admitted.  No
+    model runs: K/V contents are whatever the pool holds, and the window
+    queries come from `q_window(n)`.
+    """
+
+    def __init__(self, pool: BlockPool, requests, block: int, bt_stride: int):
+        self.pool, self.block, self.bt_stride = pool, block, bt_stride
+        self.requests = [(i, int(p), int(g)) for i, (p, g) in enumerate(requests)]
+        self.waiting = list(self.requests)
+        self.running = {}          # request id -> [length, tokens left, table row (ids in logical order)]
+        self.finished = []
+        self.tokens = 0
+
+    def _blocks(self, length: int) -> int:
+        return (length + self.block - 1) // self.block
+
+    def outstanding(self) -> int:
+        """Blocks the running sequences may still take, without compression."""
+        return sum(self._blocks(L + left) - len(row) for L, left, row in self.running.values())
+
+    def admit(self) -> int:
+        n = 0
+        spare = len(self.pool.free) - self.outstanding()
+        while self.waiting:
+            rid, prompt, gen = self.waiting[0]
+            need = self._blocks(prompt + gen)
+            if need > spare or need > self.bt_stride:
+                break
+            self.waiting.pop(0)
+            self.running[rid] = [prompt, gen, self.pool.take(self._blocks(prompt))]
+            spare -= need
+            n += 1
+        return n
+
+    def step(self) -> int:
+        """One decode step; returns the tokens decoded."""
+        done = []
+        for rid, st in self.running.items():
+            L, left, row = st
+            if L % self.block == 0:
+                row.append(self.pool.take(1)[0])
+            st[0], st[1] = L + 1, left - 1
+            if st[1] == 0:
+                done.append(rid)
+        for rid in done:
+            self.pool.give(self.running.pop(rid)[2])
+            self.finished.append(rid)
+        decoded = len(self.running) + len(done)
+        self.tokens += decoded
+        return decoded
+
+    def compress(self, comp, schedule: PeriodicSchedule, q_window) -> int:
+        """Compress the schedule's choice among the running sequences; returns
+        the blocks freed."""
+        ids = sorted(self.running)
+        if not ids:
+            return 0
+        lengths = [self.running[r][0] for r in ids]
+        pick = schedule.choose(lengths)
+        # fresh blocks leave the pool before the old ones come back: keep the
+        # longest prefix of the choice the spare blocks can cover
+        if pick:
+            nn = comp.plan(torch.tensor([lengths[i] for i in pick], dtype=torch.int32), self.bt_stride)[0]
+            spare = len(self.pool.free) - self.outstanding()
+            keep, need = [], 0
+            for j, i in enumerate(pick):
+                need += int(nn[j])
+                if need > spare:
+                    break
+                keep.append(i)
+            pick = keep
+        if not pick:
+            return 0
+        table = torch.full((len(ids), self.bt_stride), -1, dtype=torch.int32)
+        for i, r in enumerate(ids):
+            row = self.running[r][2]
+            table[i, :len(row)] = torch.tensor(row, dtype=torch.int32)
+        freed, status = compress_selected(comp, pick, lengths, table, q_window(len(pick)), self.pool)
+        if status != 0:
+            raise RuntimeError(f"compression failed: {kara.status_string(status)}")
+        for i in pick:
+            r = ids[i]
+            L = int(lengths[i])
+            self.running[r][0] = L
+            self.running[r][2] = [int(x) for x in table[i, :self._blocks(L)]]
+        return len(freed)
+
+    def live_blocks(self) -> list[int]:
+        return [b for st in self.running.values() for b in st[2]]
