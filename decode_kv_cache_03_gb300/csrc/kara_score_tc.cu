@@ -75,6 +75,7 @@ struct Shared {
     uint32_t tmem_base;
     int abort;
     int bad;
+    int32_t sblk[kSlice / 16 + 2];  // block ids of this CTA's key slice (16-token blocks)
 };
 
 // Dynamic shared memory of one CTA.  Never below 120 KB: with more than half
@@ -306,11 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const int32_t ws = L - g.W;
     const int32_t *btr = g.bt + (int64_t)s * g.bt_stride;
+    // every block of the window is checked; the slice's own ids are kept in
+    // shared memory, so the gather below issues its copies without waiting on
+    // table loads
+    const int fb = (ws + slice0) / g.bs;  // first logical block of the slice
     if (valid) {
         const int nb = (L + g.bs - 1) / g.bs - ws / g.bs;
+        const int nbs = (ws + slice0 + S - 1) / g.bs - fb + 1;
         for (int t = threadIdx.x; t < nb; t += kThreads) {
-            const int32_t b = btr[ws / g.bs + t];
+            const int lb = ws / g.bs + t;
+            const int32_t b = btr[lb];
             if (b < 0 || b >= g.num_blocks) sh->bad = 1;
+            if (lb >= fb && lb < fb + nbs) sh->sblk[lb - fb] = b;
         }
     }
     __syncthreads();
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int idx = threadIdx.x; idx < S * CPR; idx += kThreads) {
             const int r = idx / CPR, cc = idx % CPR;
             const int x = ws + slice0 + r;
-            const int32_t blk = btr[x / g.bs];
+            const int32_t blk = sh->sblk[x / g.bs - fb];
             const uint16_t *src = g.k + pool_off(g, l, blk, h, x % g.bs) + cc * 8;
             const int a = cc >> 3, c8 = cc & 7;
             const uint32_t dst = sK_u + a * C_::kKAtomBytes + r * 128 + ((c8 ^ (r & 7)) << 4);
