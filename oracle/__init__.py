@@ -64,6 +64,7 @@ def lib():
                                   ctypes.c_int, ctypes.c_int, P, P]
         _lib.kro_compact.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, ctypes.c_int64, P, P]
         _lib.kro_max_threads.restype = ctypes.c_int
+        _lib.kro_compact_queries.argtypes = [ctypes.POINTER(Shape), P, P, P]
         _lib.kro_decode_attention.argtypes = [ctypes.POINTER(Shape), ctypes.c_int, P, P, P, P, P, P, ctypes.c_int]
     return _lib
 
@@ -176,6 +177,18 @@ def decode_attention(shape: Shape, layer: int, q, kpool, vpool, block_table, len
     if st != OK:
         raise ValueError(f"oracle decode attention failed: status {st}")
     return out
+
+
+def compact_queries(shape: Shape, q_ring, lengths, kept):
+    """The query ring [n_seq][layers][hq][W][d] (bf16 bits) after the step
+    moves the kept and buffer queries with K and V; returns a new array."""
+    qa = _np(q_ring, np.uint16).copy()
+    ln = _np(lengths, np.int32)
+    kp = _np(kept, np.int32)
+    st = lib().kro_compact_queries(ctypes.byref(shape), _ptr(qa), _ptr(ln), _ptr(kp))
+    if st != OK:
+        raise ValueError(f"oracle query compaction failed: status {st}")
+    return qa
 
 
 SELECT_TOKEN2CHUNK, SELECT_TOP_R, SELECT_FIXED_CHUNK = 0, 1, 2

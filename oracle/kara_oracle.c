@@ -511,6 +511,45 @@ int kro_plan(int n, const int32_t *len, int W, int B, int R, int bs, int bt_stri
 }
 
 /*
+ * Compaction of the window-query ring (reading of the survey's "query-window
+ * ring buffer": the pages are silent on where window queries live).  Each
+ * (sequence, layer, query head) keeps the queries of its last W positions in
+ * a ring of W rows, the query of logical position x in row x mod W.  When the
+ * step compacts K and V, the queries of the rows it keeps move with them, to
+ * the same new positions (kept row r to ws + r, buffer row b to ws + R + b):
+ *     ring[(ws + r) mod W]     <- old ring[(ws + kept[r]) mod W],  r < R
+ *     ring[(ws + R + b) mod W] <- old ring[(L - B + b) mod W],     b < B
+ * where kept is the window's (KV head g = h / G) retained set.  All other
+ * rows are left as they are (they belong to positions past L', which decoding
+ * overwrites).  Reading: the queries keep their stored values, as K does.
+ * q: bf16 bits [n_seq][layers][hq][W][d], modified in place; len: lengths
+ * before the step; kept: [n_seq][layers][hkv][R].
+ */
+int kro_compact_queries(const kro_shape *sh, uint16_t *q, const int32_t *len, const int32_t *kept)
+{
+    const int W = sh->W, B = sh->B, R = sh->R, D = sh->d, G = sh->hq / sh->hkv;
+    if (W < 1 || B < 0 || B >= W || R < 1 || R > W - B || sh->hq % sh->hkv) return KRO_EINVAL;
+    for (int s = 0; s < sh->n_seq; ++s)
+        if (len[s] < W) return KRO_EINVAL;
+    uint16_t *old = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)W * D);
+    for (int s = 0; s < sh->n_seq; ++s) {
+        const int64_t L = len[s], ws = L - W;
+        for (int l = 0; l < sh->layers; ++l)
+            for (int h = 0; h < sh->hq; ++h) {
+                uint16_t *ring = q + (((int64_t)s * sh->layers + l) * sh->hq + h) * W * D;
+                const int32_t *kp = kept + (((int64_t)s * sh->layers + l) * sh->hkv + h / G) * R;
+                memcpy(old, ring, sizeof(uint16_t) * (size_t)W * D);
+                for (int r = 0; r < R; ++r)
+                    memcpy(ring + ((ws + r) % W) * D, old + ((ws + kp[r]) % W) * D, sizeof(uint16_t) * (size_t)D);
+                for (int b = 0; b < B; ++b)
+                    memcpy(ring + ((ws + R + b) % W) * D, old + ((L - B + b) % W) * D, sizeof(uint16_t) * (size_t)D);
+            }
+    }
+    free(old);
+    return KRO_OK;
+}
+
+/*
  * Gather-compaction and block-table rewrite (summary section 3: Kara adapted
  * to PagedAttention, so the retained K/V must land in paged blocks).
  *
