@@ -234,6 +234,8 @@ def main():
     ap.add_argument("--select-mode", default="token2chunk", choices=["token2chunk", "top_r", "fixed_chunk"],
                     help="selection variant (top_r and fixed_chunk are the ablations of Token2Chunk)")
     ap.add_argument("--chunk", type=int, default=0, help="chunk length for --select-mode fixed_chunk")
+    ap.add_argument("--q-ring", action="store_true",
+                    help="treat the window queries as a ring and add kara_compact_queries to every step")
     ap.add_argument("--layers", type=int, default=None, help="override the workload's layer count")
     ap.add_argument("--profile-kernel", choices=["score", "select", "compact"], default=None,
                     help="only run one entry point `--steps` times (for ncu captures); prints no JSON")
@@ -289,11 +291,15 @@ def main():
     ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     for row in ev:                         # torch creates the CUDA event on its first record
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+    # --q-ring: the window queries are a ring (row = position mod W) that each step
+    # compacts with K/V; kept goes to a caller buffer for kara_compact_queries
+    kept_buf = (torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.R, dtype=torch.int32, device=dev)
+                if args.q_ring else None)
 
     if args.profile_kernel:
         profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err)
@@ -301,7 +307,12 @@ def main():
 
     def step(events=None):
         bt.copy_(bt0)                      # every step compresses the same trailing windows
-        kara.kara_compress_batch(c, p, b, fresh, freed, new_len, ws, err, stream=stream, phase_events=events)
+        kara.kara_compress_batch(c, p, b, fresh, freed, new_len, ws, err, kept_out=kept_buf, stream=stream,
+                                 phase_events=events[:5] if events else None)
+        if args.q_ring:
+            kara.kara_compact_queries(c, p, b, kept_buf, err, stream)
+            if events:
+                events[5].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -326,6 +337,7 @@ def main():
     score_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
     select_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
     compact_ms = statistics.mean(ev[i][3].elapsed_time(ev[i][4]) for i in range(args.steps))
+    qring_ms = statistics.mean(ev[i][4].elapsed_time(ev[i][5]) for i in range(args.steps)) if args.q_ring else None
     status = kara.kara_get_error(err)
     if status != 0:
         raise SystemExit(f"compression reported {kara.status_string(status)}")
@@ -352,7 +364,9 @@ def main():
         d_len.copy_(h_len, non_blocking=True)
         bt.copy_(h_bt, non_blocking=True)
         d_fresh.copy_(h_fresh, non_blocking=True)
-        kara.kara_compress_batch(c, p, b_e2e, d_fresh, freed, new_len, ws, err, stream=stream)
+        kara.kara_compress_batch(c, p, b_e2e, d_fresh, freed, new_len, ws, err, kept_out=kept_buf, stream=stream)
+        if args.q_ring:
+            kara.kara_compact_queries(c, p, b_e2e, kept_buf, err, stream)
         h_bt_out.copy_(bt, non_blocking=True)
         h_len_out.copy_(new_len, non_blocking=True)
         h_freed.copy_(freed, non_blocking=True)
@@ -401,7 +415,12 @@ def main():
         "gpu_launches": None,
         "clocks": clocks,
     }
-    line["gpu_launches"] = args.steps * launches_per_step()
+    line["gpu_launches"] = args.steps * (launches_per_step() + (1 if args.q_ring else 0))
+    if args.q_ring:
+        qbytes = nwin * spec.G * (spec.R + spec.B) * spec.d * 2 * 2
+        line["phases_ms"]["compact_queries"] = qring_ms
+        line["phases_ms"]["compact_queries_gbs"] = qbytes / (qring_ms * 1e-3) / 1e9
+        line["config"]["q_ring"] = "window queries kept as a ring and compacted every step"
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         sample_seqs = list(range(min(2, spec.n_seq)))
         bt.copy_(bt0)

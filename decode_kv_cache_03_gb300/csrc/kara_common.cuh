@@ -74,6 +74,10 @@ size_t score_scratch_bytes(const Geo &g);
 cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const int32_t *len, const int32_t *bt,
                           int32_t bt_stride, const void *q, float *out, void *ws, int32_t *err, cudaStream_t st);
 size_t decode_workspace_bytes(const kara_cache *c, int32_t n, int32_t bt_stride);
+cudaError_t launch_qring_compact(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                 const int32_t *kept, int32_t *err, cudaStream_t st);
+cudaError_t launch_qring_append(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                const void *q_new, cudaStream_t st);
 int decode_max_splits(int32_t bt_stride, int32_t block_size);
 cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
 

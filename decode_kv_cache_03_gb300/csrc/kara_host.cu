@@ -200,6 +200,33 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
     return cuda_status(launch_score(g, scores, ws, err, (cudaStream_t)stream));
 }
 
+kara_status kara_compact_queries(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                 const int32_t *kept, int32_t *err, kara_stream_t stream)
+{
+    kara_status st = check_params(p);
+    if (st != KARA_OK) return st;
+    st = check_cache(c);
+    if (st != KARA_OK) return st;
+    if (!b || b->n < 0) return KARA_EINVAL;
+    if (b->n == 0) return KARA_OK;
+    if (!b->len || !b->q || !kept || !err || !aligned16(b->q)) return KARA_EINVAL;
+    if ((int64_t)b->n * c->num_layers * c->num_q_heads > 0x7fffffffLL) return KARA_EUNSUPPORTED;
+    return cuda_status(launch_qring_compact(c, p, b, kept, err, (cudaStream_t)stream));
+}
+
+kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const kara_batch *b, const void *q_new,
+                                kara_stream_t stream)
+{
+    kara_status st = check_params(p);
+    if (st != KARA_OK) return st;
+    st = check_cache(c);
+    if (st != KARA_OK) return st;
+    if (!b || b->n < 0) return KARA_EINVAL;
+    if (b->n == 0) return KARA_OK;
+    if (!b->len || !b->q || !q_new || !aligned16(b->q) || !aligned16(q_new)) return KARA_EINVAL;
+    return cuda_status(launch_qring_append(c, p, b, q_new, (cudaStream_t)stream));
+}
+
 size_t kara_decode_workspace_size(const kara_cache *c, int32_t n, int32_t bt_stride)
 {
     if (check_cache(c) != KARA_OK || n < 0 || bt_stride < 1) return 0;

@@ -69,6 +69,8 @@ def _load():
         "kara_get_error": ([P, P], ctypes.c_int),
         "kara_compact_static": ([PC, PP, PB, P, P, I64, P, P, P, P], ctypes.c_int),
         "kara_decode_workspace_size": ([PC, I32, I32], SZ),
+        "kara_compact_queries": ([PC, PP, PB, P, P, P], ctypes.c_int),
+        "kara_append_queries": ([PC, PP, PB, P, P], ctypes.c_int),
         "kara_decode_attention": ([PC, I32, I32, P, P, I32, P, P, P, SZ, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -81,7 +83,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("kara_status_string", "kara_version", "kara_plan", "kara_workspace_size", "kara_score",
             "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error", "kara_compact_static",
-            "kara_decode_workspace_size", "kara_decode_attention")
+            "kara_decode_workspace_size", "kara_decode_attention", "kara_compact_queries", "kara_append_queries")
 STATIC_MAX_SEQS = 8192     # KARA_STATIC_MAX_SEQS
 
 
@@ -148,6 +150,19 @@ def kara_score(c: Cache, p: Params, b: Batch, scores: torch.Tensor, ws: torch.Te
                stream=None):
     _check(_lib.kara_score(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(scores), _ptr(ws),
                            ws.numel() * ws.element_size(), _ptr(err), _stream(stream)), "kara_score")
+
+
+def kara_compact_queries(c: Cache, p: Params, b: Batch, kept: torch.Tensor, err: torch.Tensor, stream=None):
+    """Move the kept and buffer queries of the ring b.q with the step's K/V compaction."""
+    _check(_lib.kara_compact_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(kept), _ptr(err),
+                                     _stream(stream)), "kara_compact_queries")
+
+
+def kara_append_queries(c: Cache, p: Params, b: Batch, q_new: torch.Tensor, stream=None):
+    """Write one decode step's queries [n][layers][hq][D] into row len mod W of each ring."""
+    assert q_new.dtype == torch.bfloat16 and q_new.is_contiguous()
+    _check(_lib.kara_append_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), _ptr(q_new),
+                                    _stream(stream)), "kara_append_queries")
 
 
 def kara_decode_workspace_size(c: Cache, n: int, bt_stride: int) -> int:

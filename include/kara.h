@@ -157,6 +157,38 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
                        kara_stream_t stream);
 
 /*
+ * The window-query ring (the pages do not say where window queries live;
+ * summary section 1 "Mechanism": the queries of all W window tokens score the
+ * window).  b->q may hold, per (sequence, layer, query head), the queries of
+ * the last W positions in a ring of W rows, the query of logical position x in
+ * row x mod W.  Bidirectional scores do not depend on the order of the query
+ * rows, so kara_score and kara_compress_batch read the ring as it stands
+ * (score_mode KARA_SCORE_BIDIRECTIONAL; the causal ablation needs the rows in
+ * position order).
+ *
+ * kara_compact_queries: after kara_compact / kara_compress_batch, moves the
+ * queries of the kept rows and of the protected buffer to their new positions,
+ * in place:  row (ws + r) mod W <- row (ws + kept[r]) mod W for r < R, and
+ * row (ws + R + b) mod W <- row (L - B + b) mod W for b < B, where L is the
+ * length before the step (b->len, as passed to the step) and kept is the
+ * step's output.  Other rows are left as they are (positions past L', which
+ * decoding overwrites).  Nothing moves if *err is non-zero (the step failed);
+ * a kept row that is not strictly increasing in [0, C) records KARA_EINVAL and
+ * leaves that window's queries as they are.  The next compression of a
+ * sequence sees the queries of its whole window only if at least C - R tokens
+ * were decoded since the last one (earlier positions' queries have left the
+ * ring).
+ *
+ * kara_append_queries: one decode step; q_new [n][num_layers][num_q_heads][D]
+ * (bf16, device) goes to row len[s] mod W of each ring, len[s] being the new
+ * token's position (the length before the append).
+ */
+kara_status kara_compact_queries(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                 const int32_t *kept, int32_t *err, kara_stream_t stream);
+kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const kara_batch *b,
+                                const void *q_new, kara_stream_t stream);
+
+/*
  * Decode attention over the paged cache (summary section 3: Kara adapted to
  * PagedAttention; the blocks a compression frees serve more decoding
  * sequences).  It reads K and V through the same block table that
