@@ -49,10 +49,17 @@ using namespace ptx;
 
 constexpr int kSlice = 256;        // keys per CTA
 constexpr int kStrip = 128;        // query rows per strip
-constexpr int kThreads = 320;
-constexpr int kSoftThreads = 256;  // warps 2..9
 constexpr int kMaxStages = 4;
-constexpr int kMaxRowsPerThread = 32;  // (G*W rounded up to 128) / 256, G*W <= 8192
+constexpr int kMaxGW = 8192;       // query rows per window (G*W) the kernel supports
+
+// Warp roles: warp 0 issues TMA, warp 1 issues MMAs, then 4*NG softmax warps in
+// NG column groups (four warps per group cover the 128 TMEM lanes).
+template <int NG>
+struct Roles {
+    static constexpr int kSoft = 128 * NG;        // softmax threads
+    static constexpr int kThreads = 64 + kSoft;
+    static constexpr int kRows = kMaxGW / kSoft;  // query rows per softmax thread, at most
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s: every wait here normally ends in microseconds
 
@@ -84,10 +91,10 @@ struct Shared {
 // while that peer waits for it at a cluster barrier.
 constexpr size_t kMinSmem = 120 * 1024;
 
-size_t smem_bytes(int D, int T, int stages)
+size_t smem_bytes(int D, int T, int stages, int NG)
 {
     const size_t kb = (size_t)kSlice * D * 2, qb = (size_t)kStrip * D * 2;
-    const size_t need = 1024 + kb + stages * qb + (size_t)T * kStrip * 8 + sizeof(Shared);
+    const size_t need = 1024 + kb + stages * qb + (size_t)T * kStrip * 4 * NG + sizeof(Shared);
     return need > kMinSmem ? need : kMinSmem;
 }
 
@@ -183,52 +190,61 @@ __device__ __forceinline__ float sum_pairs(const uint64_t (&acc)[4])
     return s;
 }
 
-// Merges the per-half-slice log2-sum-exp pairs of query rows r0, r0 + 256,
-// ... below r_hi over the cluster's ncta slices and stores
-// -lse2 = -log2 sum 2^(l - max) - max into the .x field of the row's pair in
+// Merges the NG per-column-group log2-sum-exp values of query rows r0,
+// r0 + kSoft, ... below r_hi over the cluster's ncta slices and stores
+// -lse2 = -log2 sum 2^(l - max) - max into the first value of the row in
 // every CTA.  NR rows at a time, all NR * ncta remote loads in flight before
 // any is used.
-template <int NR, int NP>
+template <int NR, int NP, int NG>
 __device__ __forceinline__ void merge_rows(uint32_t part_u32, int r0, int r_hi, int ncta)
 {
-    for (; r0 < r_hi; r0 += NR * kSoftThreads) {
-        float2 pr[NR][NP];
+    constexpr int kSoft = Roles<NG>::kSoft;
+    for (; r0 < r_hi; r0 += NR * kSoft) {
+        float pr[NR][NP][NG];
 #pragma unroll
         for (int k = 0; k < NR; ++k) {
-            const int r = r0 + k * kSoftThreads;
+            const int r = r0 + k * kSoft;
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (r < r_hi && cr < ncta) pr[k][cr] = ld_cluster_f2(mapa(part_u32 + 8u * r, (uint32_t)cr));
+                if (r < r_hi && cr < ncta) {
+                    static_assert(NG == 2, "two partials per row");
+                    const float2 x = ld_cluster_f2(mapa(part_u32 + 4u * NG * r, (uint32_t)cr));
+                    pr[k][cr][0] = x.x, pr[k][cr][1] = x.y;
+                }
         }
 #pragma unroll
         for (int k = 0; k < NR; ++k) {
-            const int r = r0 + k * kSoftThreads;
+            const int r = r0 + k * kSoft;
             if (r >= r_hi) continue;
             float M = -INFINITY;
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (cr < ncta) M = max3(M, pr[k][cr].x, pr[k][cr].y);
+                if (cr < ncta)
+#pragma unroll
+                    for (int q = 0; q < NG; ++q) M = fmaxf(M, pr[k][cr][q]);
             float Z = 0.f;
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (cr < ncta) Z += ex2(pr[k][cr].x - M) + ex2(pr[k][cr].y - M);
+                if (cr < ncta)
+#pragma unroll
+                    for (int q = 0; q < NG; ++q) Z += ex2(pr[k][cr][q] - M);
             const float nl = -(M + log2f(Z));
 #pragma unroll
             for (int cr = 0; cr < NP; ++cr)
-                if (cr < ncta) st_cluster_f32(mapa(part_u32 + 8u * r, (uint32_t)cr), nl);
+                if (cr < ncta) st_cluster_f32(mapa(part_u32 + 4u * NG * r, (uint32_t)cr), nl);
         }
     }
 }
 
 // Pass 1 of one softmax thread (query row `row` of every strip, the
-// NLD * 32 keys of its warp half): for each strip, waits for the S tile in
-// TMEM buffer t & 1, releases the buffer once its columns are in registers,
-// and stores log2 sum 2^l2 over those keys (shifted by their maximum) at
-// lse_half[2 * r + hf].  NLD is a template parameter so that one strip's
-// loads, maxima and exponentials form a single branch-free block.
-template <int NLD, bool CAUSAL>
-__device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta0, int row, int hf, int T, int GW,
-                                           float c2, float *lse_half, int W, int key0)
+// NLD * 32 keys of its column group cg): for each strip, waits for the S tile
+// in TMEM buffer t & 1, releases the buffer once its columns are in
+// registers, and stores log2 sum 2^l2 over those keys (shifted by their
+// maximum) at lse_part[NG * r + cg].  NLD is a template parameter so that one
+// strip's loads, maxima and exponentials form a single branch-free block.
+template <int NLD, bool CAUSAL, int NG>
+__device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta0, int row, int cg, int T, int GW,
+                                           float c2, float *lse_part, int W, int key0)
 {
     const int lane = threadIdx.x & 31;
     for (int t = 0; t < T; ++t) {
@@ -264,28 +280,30 @@ __device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta
 #pragma unroll
         for (int k = 0; k < NLD; ++k) exp_sum32(v[k], c2p, nmp, acc);
         const float z = sum_pairs(acc);
-        // z >= 1, as the maximum contributes 2^0.  The two halves of a row stay
-        // separate until the cluster merge, so no warp waits for another here.
+        // z >= 1, as the maximum contributes 2^0.  The column groups of a row
+        // stay separate until the cluster merge, so no warp waits for another.
         const int r = t * kStrip + row;
-        if (r < GW) lse_half[2 * r + hf] = mc + log2f(z);
+        if (r < GW) lse_part[NG * r + cg] = mc + log2f(z);
     }
 }
 
 // CAUSAL: the scoring ablation without bidirectional attention (query i sees
 // keys j <= i); a template parameter so that the default path carries no mask code.
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+// NG: column groups of softmax warps (Roles).
+template <int D, bool CAUSAL, int NG>
+__global__ void __launch_bounds__(Roles<NG>::kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
                     int32_t *err, int ncta, int T, int stages, float c2)
 {
     using C_ = Cfg<D>;
+    constexpr int kSoft = Roles<NG>::kSoft, kThreads = Roles<NG>::kThreads, kRows = Roles<NG>::kRows;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sK = base;
     uint8_t *sQ = sK + C_::kKBytes;
-    float2 *part = reinterpret_cast<float2 *>(sQ + stages * C_::kQBytes);  // per row: the two halves' lse2
-    Shared *sh = reinterpret_cast<Shared *>(part + T * kStrip);
+    float *part = reinterpret_cast<float *>(sQ + stages * C_::kQBytes);  // per row: NG partial lse2
+    Shared *sh = reinterpret_cast<Shared *>(part + T * kStrip * NG);
     const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sh->tfull[i]), 1);
-            mbar_init(smem_u32(&sh->tempty[i]), kSoftThreads / 32);
+            mbar_init(smem_u32(&sh->tempty[i]), kSoft / 32);
         }
         mbar_init(smem_u32(&sh->done), 1);
         fence_mbarrier_init();
@@ -447,74 +465,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         cluster_wait();
     } else {
-        // ---------------- softmax / column sums (warps 2..9) -------------------
-        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        // ---------------- softmax / column sums (warps 2 ..) ---------------------
+        const int sw = warp - 2, q4 = warp & 3, cg = sw >> 2;  // TMEM lane quarter, column group
         const int row = 32 * q4 + lane;
-        const int sidx = (warp - 2) * 32 + lane;
+        const int sidx = sw * 32 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        const int nld = S >> 6;  // loads of 32 columns per warp half: 1..4
+        const int cols = S / NG;   // pass-1 keys of this column group
+        const int nld = cols >> 5; // 32-column loads: 1..4
 
-        // pass 1: per row, log2-sum-exp over this warp half's keys of the slice
-        float *lse_half = reinterpret_cast<float *>(part);
-        switch (nld) {
-        case 1: pass1_rows<1, CAUSAL>(sh, err, tmem + lane_base + hf * 32, row, hf, T, GW, c2, lse_half, g.W,
-                                  slice0 + hf * 32); break;
-        case 2: pass1_rows<2, CAUSAL>(sh, err, tmem + lane_base + hf * 64, row, hf, T, GW, c2, lse_half, g.W,
-                                  slice0 + hf * 64); break;
-        case 3: pass1_rows<3, CAUSAL>(sh, err, tmem + lane_base + hf * 96, row, hf, T, GW, c2, lse_half, g.W,
-                                  slice0 + hf * 96); break;
-        default: pass1_rows<4, CAUSAL>(sh, err, tmem + lane_base + hf * 128, row, hf, T, GW, c2, lse_half, g.W,
-                                 slice0 + hf * 128); break;
+        // pass 1: per row, log2-sum-exp over this column group's keys of the slice
+        const uint32_t ta1 = tmem + lane_base + cg * cols;
+        const int key0 = slice0 + cg * cols;
+        if (nld == 1) {
+            pass1_rows<1, CAUSAL, NG>(sh, err, ta1, row, cg, T, GW, c2, part, g.W, key0);
+        } else if (nld == 2) {
+            pass1_rows<2, CAUSAL, NG>(sh, err, ta1, row, cg, T, GW, c2, part, g.W, key0);
+        } else if (nld == 3) {
+            pass1_rows<3, CAUSAL, NG>(sh, err, ta1, row, cg, T, GW, c2, part, g.W, key0);
+        } else {
+            pass1_rows<4, CAUSAL, NG>(sh, err, ta1, row, cg, T, GW, c2, part, g.W, key0);
         }
         __syncwarp();
         cluster_arrive();
         cluster_wait();
-        // merge the half-slices' lse2 of every query row: this CTA owns rows
-        // [r_lo, r_hi), reads their pairs from every peer and writes -lse2 into
-        // the .x field of the row's pair in every peer
+        // merge the column groups' lse2 of every query row: this CTA owns rows
+        // [r_lo, r_hi), reads their NG values from every peer and writes -lse2
+        // into the first value of the row in every peer
         const int TT = T * kStrip;
         {
             const int P = (GW + ncta - 1) / ncta;
             const int r_lo = min(GW, (int)crank * P), r_hi = min(GW, r_lo + P);
             const uint32_t pa = smem_u32(part);
+            // NR * NP * NG = 64 values in flight per thread
             if (ncta <= 4)
-                merge_rows<8, 4>(pa, r_lo + sidx, r_hi, ncta);
+                merge_rows<16 / NG, 4, NG>(pa, r_lo + sidx, r_hi, ncta);
             else
-                merge_rows<4, 8>(pa, r_lo + sidx, r_hi, ncta);
+                merge_rows<8 / NG, 8, NG>(pa, r_lo + sidx, r_hi, ncta);
         }
         cluster_arrive();
         cluster_wait();
         // -lse2 of every row, packed to one float per row in place of the pairs;
         // rows past G*W (the padding of the last strip) get -inf, so they add 0
-        float nlv[kMaxRowsPerThread];
+        float nlv[kRows];
 #pragma unroll
-        for (int k = 0; k < kMaxRowsPerThread; ++k) {
-            const int r = sidx + k * kSoftThreads;
-            nlv[k] = r < GW ? part[r].x : -INFINITY;
+        for (int k = 0; k < kRows; ++k) {
+            const int r = sidx + k * kSoft;
+            nlv[k] = r < GW ? part[NG * r] : -INFINITY;
         }
-        named_barrier(1, kSoftThreads);
-        float *nlse2 = reinterpret_cast<float *>(part);
+        named_barrier(1, kSoft);
+        float *nlse2 = part;
 #pragma unroll
-        for (int k = 0; k < kMaxRowsPerThread; ++k) {
-            const int r = sidx + k * kSoftThreads;
+        for (int k = 0; k < kRows; ++k) {
+            const int r = sidx + k * kSoft;
             if (r < TT) nlse2[r] = nlv[k];
         }
-        named_barrier(1, kSoftThreads);
+        named_barrier(1, kSoft);
 
-        // pass 2: column sums with keys on TMEM lanes
+        // pass 2: column sums with keys on TMEM lanes; column group cg takes key tile cg
+        constexpr int kL2 = 4;   // 32-column loads per strip
+        const int mt = cg, c0 = 0;
         float acc = 0.f;
         for (int t = 0; t < T2; ++t) {
             const int j = T + t, b = j & 1;
             wait_phase(smem_u32(&sh->tfull[b]), (j >> 1) & 1, sh, err);
             tc_fence_after();
-            uint32_t v[4][32];
-            const bool mine = hf < nM;
+            uint32_t v[kL2][32];
+            const bool mine = mt < nM;
             if (mine) {
-                const uint32_t ta = tmem + lane_base + b * 256 + hf * 128;
+                const uint32_t ta = tmem + lane_base + b * 256 + mt * 128 + c0;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_ld32(ta + k * 32, v[k]);
+                for (int k = 0; k < kL2; ++k) tmem_ld32(ta + k * 32, v[k]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_wait_ld(v[k]);
+                for (int k = 0; k < kL2; ++k) tmem_wait_ld(v[k]);
             }
             tc_fence_before();
             __syncwarp();
@@ -523,33 +545,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (CAUSAL && mine) {
                 // key j adds the weights of queries i >= j only: column n of the
                 // strip is query i = (t*128 + n) mod W
-                const int j = slice0 + hf * 128 + row, i0 = (t * kStrip) % g.W;
+                const int jk = slice0 + mt * 128 + row, i0 = (t * kStrip) % g.W;
                 const bool wraps = i0 + kStrip > g.W;
-                const bool all_in = !wraps && i0 >= j;
-                const bool all_out = !wraps && i0 + kStrip - 1 < j;
+                const bool all_in = !wraps && i0 >= jk;
+                const bool all_out = !wraps && i0 + kStrip - 1 < jk;
                 skip = __all_sync(0xffffffffu, all_out);
                 if (!skip && !__all_sync(0xffffffffu, all_in)) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                    for (int k = 0; k < kL2; ++k)
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
-                            int i = i0 + k * 32 + c;
+                            int i = i0 + c0 + k * 32 + c;
                             if (i >= g.W) i -= g.W;
-                            if (i < j) v[k][c] = 0xff800000u;
+                            if (i < jk) v[k][c] = 0xff800000u;
                         }
                 }
             }
             if (mine && !skip) {
-                const float *nl = nlse2 + t * kStrip;
+                const float *nl = nlse2 + t * kStrip + c0;
                 uint64_t pacc[4] = {0, 0, 0, 0};
                 const uint64_t c2p = pack2(c2, c2);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) exp_sum32_cols(v[k], c2p, nl + k * 32, pacc);
+                for (int k = 0; k < kL2; ++k) exp_sum32_cols(v[k], c2p, nl + k * 32, pacc);
                 acc += sum_pairs(pacc);
             }
         }
-        const int key = slice0 + hf * 128 + row;
-        if (hf < nM && key < g.C) scores[u * g.C + key] = acc;
+        const int key = slice0 + mt * 128 + row;
+        if (mt < nM && key < g.C) scores[u * g.C + key] = acc;
     }
 
     __syncthreads();
@@ -579,9 +601,13 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
 {
     const int ncta = (g.W + kSlice - 1) / kSlice;
     const int T = (g.G * g.W + kStrip - 1) / kStrip;
+    // Two column groups of softmax warps.  Four (16 softmax warps) made pass 1
+    // 7 % faster but pass 2 13 % slower on the Qwen3-14B shape: with four busy
+    // softmax warps per SM sub-partition, the MMA-issuing warp falls behind.
+    constexpr int NG = 2;
     int stages = kMaxStages;
-    while (stages > 2 && smem_bytes(D, T, stages) > 232448) --stages;
-    const size_t smem = smem_bytes(D, T, stages);
+    while (stages > 2 && smem_bytes(D, T, stages, NG) > 232448) --stages;
+    const size_t smem = smem_bytes(D, T, stages, NG);
     if (smem > 232448) return cudaErrorInvalidValue;
 
     auto fn = encode_fn();
@@ -597,12 +623,12 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-    auto kern = g.causal ? score_tc_kernel<D, true> : score_tc_kernel<D, false>;
+    auto kern = g.causal ? score_tc_kernel<D, true, NG> : score_tc_kernel<D, false, NG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(g.nwin * ncta));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Roles<NG>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
