@@ -70,6 +70,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` bytes (a multiple of 16; both
+// addresses 16-byte aligned) on the bulk-copy engine; completes `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // ---- cp.async (16-byte gathers) ---------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {

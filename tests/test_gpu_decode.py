@@ -89,3 +89,53 @@ def test_decode_reports_bad_lengths_and_blocks():
     bt[2, 1] = wl.num_blocks + 5      # outside the pool: reported, never dereferenced
     got, st = run_decode(kara, d.k, d.v, spec.hq, 0, d.lengths, bt, q)
     assert st == kara.EBADBLOCK
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_ignores_rows_past_the_end(D):
+    """The last block of each sequence holds rows past its length; they are
+    NaN here and must not reach the output (the oracle reads x < L only)."""
+    kara = lib()
+    spec = random_spec(520 + D, G=4, hkv=2, W=64, B=16, D=D, n_seq=4, layers=1, len_lo=1031, len_hi=1100)
+    wl = synth.generate(spec)
+    gen = torch.Generator().manual_seed(D)
+    short = torch.randint(65, 1031, (spec.n_seq,), generator=gen, dtype=torch.int32)
+    wl.lengths.copy_(torch.minimum(wl.lengths, short))  # shorter than generated: the table covers them
+    wl.lengths[0] = 1024 + 7                    # a ragged block right after the split boundary
+    k, v = wl.k.clone(), wl.v.clone()
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    for s in range(spec.n_seq):
+        L = int(wl.lengths[s])
+        if L % 16:
+            blk = int(wl.block_table[s, L // 16])
+            k[0, blk, :, L % 16:] = nan
+            v[0, blk, :, L % 16:] = nan
+    q = synth.decode_queries(spec, 3)
+    d = to_device(wl)
+    got, st = run_decode(kara, k.cuda(), v.cuda(), spec.hq, 0, d.lengths, d.block_table, q.cuda())
+    assert st == 0 and np.all(np.isfinite(got))
+    ref = oracle.decode_attention(oracle.shape_of(wl), 0, q, k, v, wl.block_table, wl.lengths)
+    np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
+
+
+def test_decode_reads_a_bad_block_as_zeros():
+    """A block id outside the pool is reported and its rows read as zeros: the
+    same result as the oracle over a table that points at an all-zero block."""
+    kara = lib()
+    spec = random_spec(530, G=4, hkv=2, W=64, B=16, D=128, n_seq=3, layers=1, len_lo=300, len_hi=1500)
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    q = synth.decode_queries(spec, 4)
+    bt = wl.block_table.clone()
+    bt[1, 3] = wl.num_blocks + 5
+    got, st = run_decode(kara, d.k, d.v, spec.hq, 0, d.lengths, bt.cuda(), q.cuda())
+    assert st == kara.EBADBLOCK
+    zero = torch.zeros_like(wl.k[:, :1])
+    kz, vz = torch.cat([wl.k, zero], 1), torch.cat([wl.v, zero], 1)
+    bt_ref = wl.block_table.clone()
+    bt_ref[1, 3] = wl.num_blocks
+    s = wl.spec
+    shape = oracle.make_shape(s.n_seq, s.layers, s.hq, s.hkv, s.d, s.block, s.W, s.B, s.K, s.R, s.lam,
+                              wl.bt_stride, wl.num_blocks + 1)
+    ref = oracle.decode_attention(shape, 0, q, kz, vz, bt_ref, wl.lengths)
+    np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
