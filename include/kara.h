@@ -203,7 +203,11 @@ kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const
  * ws/ws_bytes: at least kara_decode_workspace_size(c, n, bt_stride) bytes.
  * err: device int32; a length outside [1, bt_stride*block_size] records
  * KARA_EINVAL and that sequence's output is 0; a block id outside the pool
- * records KARA_EBADBLOCK (the row is read as zeros, never from outside the pool).
+ * records KARA_EBADBLOCK (the row is read as zeros, never from outside the pool);
+ * K/V slices are staged through shared memory behind bounded waits, and one
+ * that runs out records KARA_ETIMEOUT (outputs are then unspecified).
+ * Layout: each (block, KV head) slice of a pool must be block_size * head_dim
+ * contiguous bf16 (rows at stride head_dim), as in the layout above.
  * Supported: the kara_cache shapes above; n <= 65535.
  */
 size_t kara_decode_workspace_size(const kara_cache *c, int32_t n, int32_t bt_stride);
