@@ -1,5 +1,6 @@
-// Inline-PTX wrappers for sm_100-family features used by the scoring kernel:
-// mbarrier, TMA (cp.async.bulk.tensor), tcgen05 (MMA, TMEM), clusters, DSMEM.
+// Inline-PTX wrappers for sm_100-family features used by the kernels:
+// mbarrier, TMA (cp.async.bulk.tensor, cp.async.bulk), tcgen05 (MMA, TMEM),
+// clusters, DSMEM.
 // Internal header of the Kara sm_103a library.
 #pragma once
 
@@ -259,8 +260,8 @@ __device__ __forceinline__ float max3(float a, float b, float c)
 // in fp32 Horner form with fused multiply-adds its relative error stays below
 // 3e-6.  2^n is applied by adding n to the exponent field.  Inputs are clamped
 // at -126 so the exponent never underflows (2^-126 stands in for anything
-// smaller, as the flush-to-zero ex2 gives 0 there).  Used for a share of the
-// exponentials so that the special-function unit is not the only exp engine.
+// smaller, as the flush-to-zero ex2 gives 0 there).  An FMA-pipe alternative
+// to ex2; the scoring kernel measured it slower and does not call it.
 constexpr float kExp2C0 = 0.99999928474426270f;
 constexpr float kExp2C1 = 0.69312179088592530f;
 constexpr float kExp2C2 = 0.24024744331836700f;
