@@ -130,9 +130,10 @@ class ClockSampler:
         return out
 
 
-def cpu_oracle_sample(wl_dev, seqs, layers_sample):
+def cpu_oracle_sample(wl_dev, seqs, layers_sample, threads=None):
     """Time the oracle (as it stands) on a bounded sample: the windows of a few
-    sequences and layers of the same workload.  Returns (windows/s, seconds, threads, windows)."""
+    sequences and layers of the same workload, on `threads` host threads (all
+    cores by default).  Returns (windows/s, seconds, threads, windows)."""
     import oracle
     sub = synth.host_subset(wl_dev, seqs)
     spec = sub.spec.with_(layers=layers_sample)
@@ -141,7 +142,7 @@ def cpu_oracle_sample(wl_dev, seqs, layers_sample):
     v = sub.v[:layers_sample].contiguous()
     sh = oracle.make_shape(spec.n_seq, spec.layers, spec.hq, spec.hkv, spec.d, spec.block, spec.W, spec.B,
                            spec.K, spec.R, spec.lam, sub.bt_stride, sub.num_blocks)
-    threads = oracle.max_threads()
+    threads = threads or oracle.max_threads()
     t0 = time.perf_counter()
     sc = oracle.scores(sh, q, k, sub.block_table, sub.lengths, nthreads=threads)
     _, kept = oracle.select_batch(sc, spec.K, spec.R, spec.lam, nthreads=threads)
@@ -438,6 +439,11 @@ def main():
         line["cpu_baseline"] = {"value": rate, "unit": "windows/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{sw} windows ({len(sample_seqs)} sequences x {nl} layers x "
                                           f"{spec.hkv} KV heads) of the same workload, {dt:.1f} s"}
+        # the same oracle on one core, over the windows of one sequence and one layer
+        rate1, dt1, _, sw1 = cpu_oracle_sample(wl, sample_seqs[:1], 1, threads=1)
+        line["cpu_baseline"]["single_core"] = {"value": rate1, "unit": "windows/s", "cores": 1,
+                                               "sample": f"{sw1} windows (1 sequence x 1 layer x {spec.hkv} KV "
+                                                         f"heads), {dt1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_ > 1:
