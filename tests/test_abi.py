@@ -115,3 +115,40 @@ def test_workspace_size_grows_with_batch(kara):
     a, b = kara.kara_workspace_size(c, p, 1), kara.kara_workspace_size(c, p, 10)
     assert 0 < a < b
     assert kara.kara_workspace_size(fake_cache(kara, head_dim=96), p, 1) == 0
+
+
+def test_decode_and_ring_argument_checks(kara):
+    """The decode-attention and query-ring entry points refuse bad arguments on
+    the host with a status; none of these calls launches anything."""
+    L = kara._lib
+    ws = ctypes.c_void_p(16)
+    c = fake_cache(kara)
+
+    def dec(cache=c, layer=0, n=1, lens=ws, bt=ws, bts=16, q=ws, out=ws, w=ws, wb=1 << 30, err=ws):
+        return L.kara_decode_attention(ctypes.byref(cache), layer, n, lens, bt, bts, q, out, w, wb, err, None)
+
+    assert dec(cache=fake_cache(kara, head_dim=96)) == kara.EUNSUPPORTED
+    assert dec(cache=fake_cache(kara, k=None)) == kara.EINVAL
+    assert dec(layer=-1) == kara.EINVAL and dec(layer=1) == kara.EINVAL    # the fake cache has 1 layer
+    assert dec(n=-1) == kara.EINVAL and dec(bts=0) == kara.EINVAL
+    assert dec(n=0) == kara.OK                                              # nothing to do
+    assert dec(lens=None) == kara.EINVAL and dec(bt=None) == kara.EINVAL and dec(err=None) == kara.EINVAL
+    assert dec(q=ctypes.c_void_p(18)) == kara.EINVAL                         # q not 16-byte aligned
+    assert dec(n=65536) == kara.EUNSUPPORTED
+    assert dec(w=None) == kara.EWORKSPACE and dec(wb=1) == kara.EWORKSPACE
+    assert kara.kara_decode_workspace_size(c, 1, 16) > 0
+
+    p = kara.params(64, 16, 8, 16, 0.1)
+    b = kara.Batch(1, 16, 16, 16, 16)
+    bn = kara.Batch(-1, 16, 16, 16, 16)
+    assert L.kara_compact_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(bn), ws, ws, None) == kara.EINVAL
+    assert L.kara_append_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(bn), ws, None) == kara.EINVAL
+    b0 = kara.Batch(0, 16, 16, 16, 16)
+    assert L.kara_compact_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b0), ws, ws, None) == kara.OK
+    assert L.kara_append_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b0), ws, None) == kara.OK
+    assert L.kara_compact_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), None, ws, None) == kara.EINVAL
+    assert L.kara_append_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), None, None) == kara.EINVAL
+    assert L.kara_append_queries(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b), ctypes.c_void_p(24),
+                                 None) == kara.EINVAL                      # q_new not 16-byte aligned
+    bad = kara.params(64, 16, 8, 0, 0.1)
+    assert L.kara_compact_queries(ctypes.byref(c), ctypes.byref(bad), ctypes.byref(b), ws, ws, None) == kara.EINVAL
