@@ -97,3 +97,39 @@ def test_full_batch(name):
         bo, so = bt2[i, xs // spec.block], xs % spec.block
         assert np.array_equal(kd[bg, :, slot].cpu().numpy().view(np.uint16), k2[0, bo, :, so])
         assert np.array_equal(vd[bg, :, slot].cpu().numpy().view(np.uint16), v2[0, bo, :, so])
+
+
+@pytest.mark.parametrize("name", ["qwen3_14b", "llama_8b"])
+def test_full_layer_decode(name):
+    """Decode attention over a whole layer of the workload, as `bench.py --decode`
+    launches it; every output is finite and the outputs of a few sampled
+    sequences equal the oracle's, recomputed from host copies of their blocks."""
+    kara = lib()
+    spec = synth.SPECS[name].with_(layers=1)
+    wl = synth.generate(spec, device="cuda", alias_prefix=False, with_q=False)
+    q = synth.decode_queries(spec, 0, device="cuda")
+    c = kara.cache(wl.k, wl.v, spec.hq)
+    n, bts = wl.block_table.shape
+    ws = torch.empty(kara.kara_decode_workspace_size(c, n, bts), dtype=torch.uint8, device="cuda")
+    out = torch.full((n, spec.hq, spec.d), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_decode_attention(c, 0, wl.lengths, wl.block_table, q, out, ws, err)
+    assert kara.kara_get_error(err) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+
+    seqs, _ = _sample(spec, 23)
+    bt = wl.block_table[seqs].cpu()
+    lens = wl.lengths[seqs].cpu()
+    nblk = [(int(L) + spec.block - 1) // spec.block for L in lens]
+    ids = sorted({int(bt[i, t]) for i in range(len(seqs)) for t in range(nblk[i])})
+    remap = {b: j for j, b in enumerate(ids)}
+    bt2 = torch.full_like(bt, -1)
+    for i in range(len(seqs)):
+        bt2[i, :nblk[i]] = torch.tensor([remap[int(b)] for b in bt[i, :nblk[i]]], dtype=torch.int32)
+    idx = torch.tensor(ids, dtype=torch.int64, device="cuda")
+    k2, v2 = wl.k[:, idx].cpu().contiguous(), wl.v[:, idx].cpu().contiguous()
+    shape = oracle.make_shape(len(seqs), 1, spec.hq, spec.hkv, spec.d, spec.block, spec.W, spec.B, spec.K,
+                              spec.R, spec.lam, bts, len(ids))
+    ref = oracle.decode_attention(shape, 0, q[seqs].cpu(), k2, v2, bt2, lens)
+    np.testing.assert_allclose(got[seqs], ref, atol=2e-4, rtol=1e-3)
