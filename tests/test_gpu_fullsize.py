@@ -1,6 +1,7 @@
 """Full-size workloads on the GPU, in the launch configuration the benchmark times.
 
-The whole batch goes through one kara_compress_batch call.  A few windows,
+The whole batch goes through one kara_compress_batch call (and its window-query
+ring through one kara_compact_queries call).  A few windows,
 sampled by a seeded generator, are recomputed by the oracle one by one from a
 host copy of their inputs taken before the call; every window and every
 sequence is also checked for properties that hold at any size.
@@ -97,6 +98,14 @@ def test_full_batch(name):
         bo, so = bt2[i, xs // spec.block], xs % spec.block
         assert np.array_equal(kd[bg, :, slot].cpu().numpy().view(np.uint16), k2[0, bo, :, so])
         assert np.array_equal(vd[bg, :, slot].cpu().numpy().view(np.uint16), v2[0, bo, :, so])
+    # --- the window queries kept as a ring, compacted with K and V over the whole
+    # batch (as `bench.py --q-ring` runs it): the sampled sequences' rings, all
+    # layers and heads, equal the oracle's compaction of their host copies
+    kara.kara_compact_queries(c, p, b, kept, err)
+    assert kara.kara_get_error(err) == 0
+    ref_ring = oracle.compact_queries(oracle.shape_of(sub), sub.q, sub.lengths, kp[seqs])
+    got_ring = wl.q[seqs].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got_ring, ref_ring)
 
 
 @pytest.mark.parametrize("name", ["qwen3_14b", "llama_8b"])
