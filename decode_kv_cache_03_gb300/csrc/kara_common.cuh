@@ -3,10 +3,38 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kara.h"
 
 namespace kara {
+
+// Failure-detection knob for tests.  With KARA_DEBUG_STALL=1 in the
+// environment, the kernels that stage data through shared memory issue no
+// copies at all, so every wait on data runs out -- after wait_ns = 1 ms
+// instead of the normal limit -- and the call reports KARA_ETIMEOUT.  Nothing
+// is in flight when those waits give up, and the waits that drain in-flight
+// work keep the normal limit.
+struct Stall {
+    int32_t on;
+    uint64_t wait_ns;
+};
+
+// Named range on the host timeline of a profiler (NVTX; a no-op when no tool
+// is attached), one per public call that launches work.
+struct Range {
+    explicit Range(const char *name);
+    ~Range();
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
+
+inline Stall debug_stall(uint64_t normal_ns)
+{
+    const char *v = getenv("KARA_DEBUG_STALL");
+    const bool on = v && v[0] == '1' && v[1] == 0;
+    return Stall{on ? 1 : 0, on ? 1000000ull : normal_ns};
+}
 
 // Per-sequence plan produced on the device by plan_kernel (summary section 3:
 // the trailing blocks of a sequence are rebuilt and the old ones released).

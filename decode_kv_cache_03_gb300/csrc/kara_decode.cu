@@ -51,6 +51,8 @@ struct DecodeArgs {
     float2 *stat;        // [n][hq][max_splits]: (max, sum) in the log2 domain
     float *out;          // [n][hq][D]
     float scale2;        // log2(e) / sqrt(D)
+    int32_t stall;       // debug: the producer issues nothing (see debug_stall)
+    uint64_t wait_ns;    // limit of the waits on progress
 };
 
 __device__ __forceinline__ bool length_ok(const DecodeArgs &a, int32_t L)
@@ -68,9 +70,10 @@ struct DecShared {
     int32_t abort;
 };
 
-// Bounded wait on phase `parity` of `bar`.  Gives up after kDecTimeoutNs,
-// or when another warp of the CTA gave up, recording KARA_ETIMEOUT.
-__device__ bool dwait(uint32_t bar, uint32_t parity, DecShared *sh, int32_t *err, bool honour_abort = true)
+// Bounded wait on phase `parity` of `bar`.  Gives up after limit_ns, or when
+// another warp of the CTA gave up, recording KARA_ETIMEOUT.
+__device__ bool dwait(uint32_t bar, uint32_t parity, DecShared *sh, int32_t *err, uint64_t limit_ns,
+                      bool honour_abort = true)
 {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -80,7 +83,7 @@ __device__ bool dwait(uint32_t bar, uint32_t parity, DecShared *sh, int32_t *err
             const uint64_t now = ptx::globaltimer();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kDecTimeoutNs) {
+            } else if (now - t0 > limit_ns) {
                 set_err(err, KARA_ETIMEOUT);
                 *(volatile int32_t *)&sh->abort = 1;
                 return false;
@@ -187,9 +190,9 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
         if (lane == 0) {
             const int64_t head_off = a.layer_off + (int64_t)g * a.head_stride;
             int issued = 0;
-            for (int j = 0; j < 2 * nb; ++j) {
+            for (int j = 0; j < (a.stall ? 0 : 2 * nb); ++j) {
                 const int st = j % kStages;
-                if (!dwait(ptx::smem_u32(&sh->empty[st]), ((j / kStages) & 1) ^ 1, sh, err)) break;
+                if (!dwait(ptx::smem_u32(&sh->empty[st]), ((j / kStages) & 1) ^ 1, sh, err, a.wait_ns)) break;
                 const int32_t blk = sh->blk[j < nb ? j : j - nb];
                 const uint32_t fb = ptx::smem_u32(&sh->full[st]);
                 if (blk < 0 || blk >= a.num_blocks) {
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
             }
             // every copy issued has landed before the CTA's shared memory is released
             for (int j = max(0, issued - kStages); j < issued; ++j)
-                dwait(ptx::smem_u32(&sh->full[j % kStages]), (j / kStages) & 1, sh, err, false);
+                dwait(ptx::smem_u32(&sh->full[j % kStages]), (j / kStages) & 1, sh, err, kDecTimeoutNs, false);
         }
         return;
     }
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     // ---- logits: lane group grp takes tokens grp + 4k of the block, 8 lanes per token
     for (int i = cw; i < nb; i += kNC) {
         const int st = i % kStages;
-        if (!dwait(ptx::smem_u32(&sh->full[st]), (i / kStages) & 1, sh, err)) break;
+        if (!dwait(ptx::smem_u32(&sh->full[st]), (i / kStages) & 1, sh, err, a.wait_ns)) break;
         const bool bad = sh->bad[st] != 0;
         const uint8_t *blkp = ring + st * BB;
         float dot[4][G];
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
         for (int d = 0; d < 2 * VW; ++d) acc[h][d] = 0ull;
     for (int i = cw; i < nb; i += kNC) {
         const int j = nb + i, st = j % kStages;
-        if (!dwait(ptx::smem_u32(&sh->full[st]), (j / kStages) & 1, sh, err)) break;
+        if (!dwait(ptx::smem_u32(&sh->full[st]), (j / kStages) & 1, sh, err, a.wait_ns)) break;
         if (sh->bad[st] == 0) {
             const int tmax = min(kBlk, nk - i * kBlk);
             if (tmax == kBlk)
@@ -419,6 +422,9 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     a.stat = reinterpret_cast<float2 *>(static_cast<char *>(ws) + align256(npart * c->head_dim * sizeof(float)));
     a.out = out;
     a.scale2 = 1.4426950408889634f / sqrtf((float)c->head_dim);
+    const Stall dbg = debug_stall(kDecTimeoutNs);
+    a.stall = dbg.on;
+    a.wait_ns = dbg.wait_ns;
     const dim3 grid((unsigned)a.max_splits, (unsigned)a.hkv, (unsigned)n);
     cudaError_t e = c->head_dim == 128 ? launch_split<128>(a, grid, err, st) : launch_split<64>(a, grid, err, st);
     if (e != cudaSuccess) return e;

@@ -3,6 +3,8 @@
 // (except kara_get_error).
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kara_common.cuh"
 
 using namespace kara;
@@ -123,6 +125,9 @@ kara_status geo_from_args(const kara_cache *c, const kara_params *p, const kara_
 }
 }  // namespace kara
 
+Range::Range(const char *name) { nvtxRangePushA(name); }
+Range::~Range() { nvtxRangePop(); }
+
 extern "C" {
 
 const char *kara_status_string(int status)
@@ -190,6 +195,7 @@ size_t kara_workspace_size(const kara_cache *c, const kara_params *p, int32_t n)
 kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_batch *b, float *scores,
                        void *ws, size_t ws_bytes, int32_t *err, kara_stream_t stream)
 {
+    const Range range("kara_score");
     Geo g;
     kara_status st = make_geo(c, p, b, &g);
     if (st != KARA_OK) return st;
@@ -203,6 +209,7 @@ kara_status kara_score(const kara_cache *c, const kara_params *p, const kara_bat
 kara_status kara_compact_queries(const kara_cache *c, const kara_params *p, const kara_batch *b,
                                  const int32_t *kept, int32_t *err, kara_stream_t stream)
 {
+    const Range range("kara_compact_queries");
     kara_status st = check_params(p);
     if (st != KARA_OK) return st;
     st = check_cache(c);
@@ -217,6 +224,7 @@ kara_status kara_compact_queries(const kara_cache *c, const kara_params *p, cons
 kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const kara_batch *b, const void *q_new,
                                 kara_stream_t stream)
 {
+    const Range range("kara_append_queries");
     kara_status st = check_params(p);
     if (st != KARA_OK) return st;
     st = check_cache(c);
@@ -237,6 +245,7 @@ kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n,
                                   const int32_t *block_table, int32_t bt_stride, const void *q, float *out,
                                   void *ws, size_t ws_bytes, int32_t *err, kara_stream_t stream)
 {
+    const Range range("kara_decode_attention");
     kara_status st = check_cache(c);
     if (st != KARA_OK) return st;
     if (layer < 0 || layer >= c->num_layers || n < 0 || bt_stride < 1) return KARA_EINVAL;
@@ -253,6 +262,7 @@ kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n,
 kara_status kara_select(const kara_params *p, int64_t n_windows, const float *scores, int32_t *cand,
                         int32_t *kept, kara_stream_t stream)
 {
+    const Range range("kara_select");
     kara_status st = check_params(p);
     if (st != KARA_OK) return st;
     if (n_windows < 0) return KARA_EINVAL;
@@ -267,6 +277,7 @@ kara_status kara_compact(const kara_cache *c, const kara_params *p, const kara_b
                          const int32_t *kept, const int32_t *fresh, int64_t n_fresh, int32_t *freed,
                          int32_t *new_len, int32_t *err, void *ws, size_t ws_bytes, kara_stream_t stream)
 {
+    const Range range("kara_compact");
     Geo g;
     kara_status st = make_geo(c, p, b, &g);
     if (st != KARA_OK) return st;
@@ -289,6 +300,7 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
                                 size_t ws_bytes, int32_t *err, kara_stream_t stream,
                                 void *const *phase_events)
 {
+    const Range range("kara_compress_batch");
     Geo g;
     kara_status st = make_geo(c, p, b, &g);
     if (st != KARA_OK) return st;

@@ -82,6 +82,7 @@ struct Shared {
     uint32_t tmem_base;
     int abort;
     int bad;
+    uint64_t wait_ns;               // limit of the waits on progress (debug_stall)
     int32_t sblk[kSlice / 16 + 2];  // block ids of this CTA's key slice (16-token blocks)
 };
 
@@ -110,7 +111,7 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *e
             const uint64_t now = globaltimer();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kTimeoutNs) {
+            } else if (now - t0 > (honour_abort ? sh->wait_ns : kTimeoutNs)) {
                 set_err(err, KARA_ETIMEOUT);
                 *(volatile int *)&sh->abort = 1;
                 return false;
@@ -293,7 +294,7 @@ __device__ __forceinline__ void pass1_rows(Shared *sh, int32_t *err, uint32_t ta
 template <int D, bool CAUSAL, int NG>
 __global__ void __launch_bounds__(Roles<NG>::kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Geo g, float *__restrict__ scores,
-                    int32_t *err, int ncta, int T, int stages, float c2)
+                    int32_t *err, int ncta, int T, int stages, float c2, uint64_t wait_ns, int stall)
 {
     using C_ = Cfg<D>;
     constexpr int kSoft = Roles<NG>::kSoft, kThreads = Roles<NG>::kThreads, kRows = Roles<NG>::kRows;
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(Roles<NG>::kThreads, 1)
     // -- validity of the window (uniform over the cluster) --------------------
     const int32_t L = g.len[s];
     bool valid = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
-    if (threadIdx.x == 0) { sh->abort = 0; sh->bad = 0; }
+    if (threadIdx.x == 0) { sh->abort = 0; sh->bad = 0; sh->wait_ns = wait_ns; }
     __syncthreads();
     const int32_t ws = L - g.W;
     const int32_t *btr = g.bt + (int64_t)s * g.bt_stride;
@@ -401,14 +402,15 @@ __global__ void __launch_bounds__(Roles<NG>::kThreads, 1)
                 tma_load_2d(sQ_u + st * C_::kQBytes + a * C_::kQAtomBytes, &tmap, fb, a * 64, row0 + t * kStrip);
             issued = j + 1;
         };
-        if (lane == 0)
+        if (lane == 0 && !stall)
             for (int j = 0; j < T + pre; ++j) produce(j);
         __syncwarp();
         cluster_arrive();
         cluster_wait();
         cluster_arrive();
         if (lane == 0) {
-            for (int j = T + pre; j < T + T2; ++j) produce(j);
+            if (!stall)
+                for (int j = T + pre; j < T + T2; ++j) produce(j);
             // drain: every issued copy has landed before this CTA may exit
             for (int j = max(0, issued - stages); j < issued; ++j)
                 wait_phase(smem_u32(&sh->full[j % stages]), (j / stages) & 1, sh, err, false);
@@ -639,7 +641,8 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const float c2 = 1.4426950408889634f / sqrtf((float)D);
-    return cudaLaunchKernelEx(&cfg, kern, tmap, g, scores, err, ncta, T, stages, c2);
+    const Stall dbg = debug_stall(kTimeoutNs);
+    return cudaLaunchKernelEx(&cfg, kern, tmap, g, scores, err, ncta, T, stages, c2, dbg.wait_ns, (int)dbg.on);
 }
 
 }  // namespace

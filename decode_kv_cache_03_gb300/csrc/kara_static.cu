@@ -50,6 +50,7 @@ extern "C" kara_status kara_compact_static(const kara_cache *c, const kara_param
                                            int32_t *freed, int32_t *new_len, int32_t *err,
                                            kara_stream_t stream)
 {
+    const Range range("kara_compact_static");
     Geo g;
     kara_status st = geo_from_args(c, p, b, &g);
     if (st != KARA_OK) return st;
