@@ -511,8 +511,9 @@ int kro_plan(int n, const int32_t *len, int W, int B, int R, int bs, int bt_stri
 }
 
 /*
- * Compaction of the window-query ring (reading of the survey's "query-window
- * ring buffer": the pages are silent on where window queries live).  Each
+ * Compaction of the window-query ring (a reading: the pages are silent on
+ * where window queries live; the gist.science summary, section 1 "Mechanism",
+ * only has the queries of all W window tokens score the window).  Each
  * (sequence, layer, query head) keeps the queries of its last W positions in
  * a ring of W rows, the query of logical position x in row x mod W.  When the
  * step compacts K and V, the queries of the rows it keeps move with them, to
