@@ -85,8 +85,8 @@ static const uint16_t *pool_row(const kro_shape *sh, const uint16_t *pool, const
 }
 
 /*
- * Window scores (summary section 1, "Mechanism" and "Rationale"; abstract:
- * "bidirectional attention to score and select").
+ * Window scores (summary section 1, "Mechanism" and "Rationale"; the
+ * abstract: KV pairs are scored and selected with bidirectional attention).
  *
  * The query states of ALL W window tokens score the keys of the window with no
  * causal mask.  For each query head h of the group and each window query i:
