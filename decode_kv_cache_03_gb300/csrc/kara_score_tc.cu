@@ -583,7 +583,10 @@ __global__ void __launch_bounds__(Roles<NG>::kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+}  // namespace
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -597,6 +600,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     });
     return fn;
 }
+
+namespace {
 
 template <int D>
 cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st)
@@ -612,7 +617,7 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
     const size_t smem = smem_bytes(D, T, stages, NG);
     if (smem > 232448) return cudaErrorInvalidValue;
 
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap tmap;
     const cuuint64_t rows = (cuuint64_t)g.n * g.layers * g.hq * g.W;
@@ -649,9 +654,15 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
 
 size_t score_scratch_bytes(const Geo &) { return 0; }
 
+bool score_sp_supported(const Geo &g);
+cudaError_t launch_score_sp(const Geo &g, float *scores, int32_t *err, cudaStream_t st);
+
 cudaError_t launch_score(const Geo &g, float *scores, void *, int32_t *err, cudaStream_t st)
 {
     if (g.nwin == 0) return cudaSuccess;
+    // one pass over the logits where the single-pass kernel covers the shape;
+    // the two-pass kernel for the causal ablation and windows above 1024 keys
+    if (score_sp_supported(g)) return launch_score_sp(g, scores, err, st);
     if (g.G * g.W > 8192) return cudaErrorInvalidValue;
     return g.D == 128 ? launch_tc<128>(g, scores, err, st) : launch_tc<64>(g, scores, err, st);
 }
