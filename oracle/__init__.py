@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kara_oracle.c")
 _LIB = os.path.join(_HERE, "libkara_oracle.so")
 
-OK, EINVAL, ENOBLOCKS, EBADBLOCK = 0, -1, -3, -6
+OK, EINVAL, ENOBLOCKS, EDUPBLOCK, EBADBLOCK = 0, -1, -3, -4, -6
 
 
 class Shape(ctypes.Structure):

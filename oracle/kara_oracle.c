@@ -52,7 +52,7 @@ typedef struct {
     int64_t layer_stride, block_stride, head_stride; /* in elements; rows are d contiguous */
 } kro_shape;
 
-enum { KRO_OK = 0, KRO_EINVAL = -1, KRO_ENOBLOCKS = -3, KRO_EBADBLOCK = -6 };
+enum { KRO_OK = 0, KRO_EINVAL = -1, KRO_ENOBLOCKS = -3, KRO_EDUPBLOCK = -4, KRO_EBADBLOCK = -6 };
 
 static double bf16_to_double(uint16_t bits)
 {
@@ -566,6 +566,16 @@ int kro_compact_queries(const kro_shape *sh, uint16_t *q, const int32_t *len, co
  * are not written.
  *
  * kept: [n_seq][layers][hkv][R]; kpool/vpool/bt are modified in place.
+ *
+ * Inputs that would make the rewrite unsound are rejected before anything is
+ * written (the pages give no rule; these follow from rebuilding into blocks
+ * the caller supplies while the old ones are still read):
+ *   - a fresh id consumed by the plan that repeats an earlier one, or that is
+ *     an entry below ceil(L/bs) of any table of the batch (a block the batch
+ *     still keeps or reads): KRO_EDUPBLOCK;
+ *   - a fresh id outside the pool: KRO_EBADBLOCK;
+ *   - a kept row that is not strictly increasing in [0, C): KRO_EINVAL
+ *     (Top-K and Token2Chunk produce ascending positions).
  */
 int kro_compact(const kro_shape *sh, uint16_t *kpool, uint16_t *vpool, int32_t *bt,
                 const int32_t *len, const int32_t *kept, const int32_t *fresh, int64_t n_fresh,
@@ -578,11 +588,25 @@ int kro_compact(const kro_shape *sh, uint16_t *kpool, uint16_t *vpool, int32_t *
     int64_t tot_new = 0;
     for (int s = 0; st == KRO_OK && s < sh->n_seq; ++s) tot_new += nn[s];
     if (st == KRO_OK && tot_new > n_fresh) st = KRO_ENOBLOCKS;
+    /* every consumed fresh id against the earlier ones and against every live
+       table entry of the batch, one pair at a time */
+    for (int64_t i = 0; st == KRO_OK && i < tot_new; ++i) {
+        for (int64_t j = 0; j < i; ++j)
+            if (fresh[j] == fresh[i]) st = KRO_EDUPBLOCK;
+        for (int s = 0; s < sh->n_seq; ++s) {
+            const int64_t nb = ((int64_t)len[s] + bs - 1) / bs;
+            for (int64_t lb = 0; lb < nb; ++lb)
+                if (bt[(int64_t)s * sh->bt_stride + lb] == fresh[i]) st = KRO_EDUPBLOCK;
+        }
+    }
     for (int64_t i = 0; st == KRO_OK && i < tot_new; ++i)
         if (fresh[i] < 0 || fresh[i] >= sh->num_blocks) st = KRO_EBADBLOCK;
-    const int64_t nk = (int64_t)sh->n_seq * sh->layers * sh->hkv * R;
-    for (int64_t i = 0; st == KRO_OK && i < nk; ++i)
-        if (kept[i] < 0 || kept[i] >= C) st = KRO_EINVAL;
+    const int64_t nwin = (int64_t)sh->n_seq * sh->layers * sh->hkv;
+    for (int64_t w = 0; st == KRO_OK && w < nwin; ++w)
+        for (int r = 0; r < R; ++r) {
+            const int32_t k = kept[w * R + r];
+            if (k < 0 || k >= C || (r > 0 && kept[w * R + r - 1] >= k)) st = KRO_EINVAL;
+        }
     if (st != KRO_OK) { free(nn); free(no); return st; }
 
     int64_t off_new = 0, off_old = 0;

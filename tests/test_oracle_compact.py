@@ -133,3 +133,44 @@ def test_compaction_rejects_short_fresh_list_and_bad_kept():
     bt[0, (L - 1) // spec.block] = wl.num_blocks + 5
     st = oracle.compact(oracle.shape_of(wl), wl.k, wl.v, bt, wl.lengths, kept, wl.fresh)[0]
     assert st == oracle.EBADBLOCK
+
+
+def test_compaction_rejects_repeated_or_live_fresh_ids():
+    """A fresh id the plan consumes must be new: not an earlier fresh id, not any
+    block the batch's tables still list (prefix blocks kept, tail blocks read)."""
+    spec = random_spec(17, W=64, B=16, D=32, n_seq=3, layers=1, R=10, len_lo=100, len_hi=180)
+    wl = synth.generate(spec)
+    sh = oracle.shape_of(wl)
+    kept = np.tile(np.arange(10, dtype=np.int32), (3, 1, spec.hkv, 1))
+    nn, _ = oracle.plan(wl.lengths, spec.W, spec.B, spec.R, spec.block, wl.bt_stride)
+    used = int(nn.sum())
+    assert oracle.compact(sh, wl.k, wl.v, wl.block_table, wl.lengths, kept, wl.fresh)[0] == oracle.OK
+
+    def status(fresh):
+        return oracle.compact(sh, wl.k, wl.v, wl.block_table, wl.lengths, kept, fresh)[0]
+
+    f = wl.fresh.clone()
+    f[used - 1] = f[0]                                   # repeated within the consumed prefix
+    assert status(f) == oracle.EDUPBLOCK
+    f = wl.fresh.clone()
+    f[1] = wl.block_table[2, 0]                          # a prefix block another sequence keeps
+    assert status(f) == oracle.EDUPBLOCK
+    L1 = int(wl.lengths[1])
+    f = wl.fresh.clone()
+    f[0] = wl.block_table[1, (L1 - 1) // spec.block]     # an old tail block the step reads
+    assert status(f) == oracle.EDUPBLOCK
+    f = wl.fresh.clone()
+    f[used:] = f[0]                                      # ids past the consumed prefix are never used
+    assert status(f) == oracle.OK
+
+
+def test_compaction_rejects_unsorted_or_repeated_kept():
+    spec = random_spec(18, W=64, B=16, D=32, n_seq=2, layers=1, R=10)
+    wl = synth.generate(spec)
+    sh = oracle.shape_of(wl)
+    kept = np.tile(np.arange(10, dtype=np.int32), (2, 1, spec.hkv, 1))
+    for mutate in (lambda k: k.__setitem__((1, 0, 1, 3), 1),            # repeats position 1
+                   lambda k: k.__setitem__((0, 0, 0, slice(4, 6)), [5, 4])):  # out of order
+        bad = kept.copy()
+        mutate(bad)
+        assert oracle.compact(sh, wl.k, wl.v, wl.block_table, wl.lengths, bad, wl.fresh)[0] == oracle.EINVAL
