@@ -20,30 +20,38 @@
 //     starts o rows into the buffer.  The G*W query rows of the window stream
 //     through a TMA ring in 128-row strips.
 //   * Per strip, S = Q_strip * K_slice^T (M = 128 rows, N = slice) goes into
-//     one of two TMEM buffers.  Each softmax thread owns one query row (TMEM
-//     lane) and half of the slice's keys.  It exponentiates its logits once,
-//     e = 2^(l2 - r) with l2 = <q,k> log2(e)/sqrt(D) and r a reference at or
-//     above their maximum, and writes e back over S in TMEM.  The two halves of
-//     a row merge their (r, sum e) in shared memory and one thread sends the
-//     CTA's partial to every CTA of the cluster with st.async (DSMEM,
-//     completing bytes on the receiver's mbarrier).
-//   * When the ncta partials of its row have arrived, the thread knows the
-//     row's normaliser Z = sum_c z_c 2^(r_c - M) exactly, reads e back from
-//     TMEM and accumulates e * 2^(r - M) / Z into registers, one accumulator
-//     per (row lane, key).  That releases the TMEM buffer for the next strip.
-//   * After the window's last strip the accumulators are summed across the 32
+//     one of two TMEM buffers.
+//   * Exponential warps (one per TMEM lane quarter; a thread owns one query row
+//     and all of the slice's keys) turn the strip's logits into
+//     e = 2^(l2 - r), l2 = <q,k> log2(e)/sqrt(D), written back over S in TMEM,
+//     and send the CTA's partial (r, z = sum e) of the row to every CTA of the
+//     cluster with st.async (DSMEM, completing bytes on the receiver's
+//     mbarrier).  The reference r is the row position's log-sum-exp from the
+//     previous strip, so no pass over the logits precedes the exponentials.
+//     A strip whose sum leaves [2^-88, 2^119] -- where the fp32 exponentials
+//     could overflow, or lose terms within 2^-30 of the row maximum -- marks
+//     its window, and an exact CUDA-core kernel recomputes marked windows
+//     afterwards (with the usual logit ranges no window is marked).
+//   * Accumulating warps (two per lane quarter, half of the keys each) wait
+//     for the ncta partials of their row, form the row's normaliser
+//     Z = sum_c z_c 2^(r_c - M) exactly, read e back from TMEM and accumulate
+//     e * 2^(r - M) / Z in registers, one fp32 accumulator per (row lane,
+//     key).  That releases the TMEM buffer for the next strip's MMA.  The
+//     exponential warps never wait for the exchange, so the exponentials of
+//     one strip overlap the exchange and accumulation of the previous one.
+//   * After a window's last strip the accumulators are summed across the 32
 //     lanes of each warp (a butterfly that leaves each lane whole keys) and
 //     across the four lane quarters through shared memory, in a fixed order.
 //
 // The kernel is persistent: each cluster walks its share of the windows, and
 // the next window's key slice loads into the second key buffer while the
 // current window is scored.  No W x W matrix and no per-row statistic reaches
-// global memory; every score is a deterministic fp32 sum.  Warp roles (384
-// threads): warp 0 issues TMA loads, warp 1 allocates TMEM and issues MMAs (one
-// lane), warps 2..3 idle, warps 4..11 are the softmax warps; the first
-// warpgroup hands most of its registers to the softmax warpgroups.  Every wait
-// is bounded; on time-out the CTA records KARA_ETIMEOUT and stops waiting,
-// still draining what it has in flight.
+// global memory; every score is a deterministic fp32 sum.  Warp roles (512
+// threads): warps 0..3 exponentials, 4..11 accumulation, 12 TMA, 13 TMEM
+// allocation and MMAs (one lane), 14..15 idle; the warpgroups trade registers
+// so the accumulating warps hold 128 accumulators each.  Every wait is bounded;
+// on time-out the CTA records KARA_ETIMEOUT and stops waiting, still draining
+// what it has in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -62,22 +70,27 @@ using namespace ptx;
 constexpr int kSlice = 256;    // keys per CTA
 constexpr int kStrip = 128;    // query rows per strip
 constexpr int kMaxCta = 4;     // CTAs per cluster: W <= 1024
-constexpr int kSlots = 3;      // exchange slots (strips in flight between CTAs)
-constexpr int kSoft = 256;     // softmax threads: two per TMEM lane
-constexpr int kThreads = 128 + kSoft;  // three warpgroups: producer/MMA, two of softmax
-// Registers per thread: at launch (65536 / 384, what ptxas assigns under the
+constexpr int kSlots = 4;      // exchange slots (strips in flight between CTAs)
+constexpr int kAcc = 256;      // accumulating threads: two per TMEM lane
+constexpr int kThreads = 512;  // warpgroups: exponentials, accumulation x2, TMA/MMA
+// Registers per thread: at launch (65536 / 512, what ptxas assigns under the
 // launch bounds), then after the warpgroups trade registers.  The trade must
-// add up: 128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch.
-constexpr int kRegsLaunch = 168;
-constexpr uint32_t kRegsLow = 40;
-constexpr uint32_t kRegsHigh = 232;
-static_assert(128 * kRegsLow + 256 * kRegsHigh == 384 * kRegsLaunch, "register trade must add up");
+// add up: 128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch.
+constexpr int kRegsLaunch = 128;
+constexpr uint32_t kRegsExp = 72;
+constexpr uint32_t kRegsAcc = 208;
+constexpr uint32_t kRegsCtl = 24;
+static_assert(128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch, "register trade must add up");
 constexpr uint32_t kTmemCols = 512;
-constexpr float kMargin = 8.f;  // log2 headroom of the reference above a chunk's maximum
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kBlockRows = 16;                         // rows of a paged block
 constexpr int kSliceBlocks = kSlice / kBlockRows + 1;  // blocks a slice can touch (17)
 constexpr int kKAtomBytes = kSliceBlocks * kBlockRows * 128;  // one 64-column atom of a key buffer
+// A row's sum of exponentials relative to its reference must lie here for the
+// fp32 exponentials to be exact to rounding: above, the largest could
+// overflow; below, terms within 2^-30 of the row maximum could flush to zero.
+constexpr float kSumLo = 3.2311742677852644e-27f;   // 2^-88
+constexpr float kSumHi = 6.6461399789245794e+35f;   // 2^119
 
 template <int D>
 struct Cfg {
@@ -92,13 +105,16 @@ struct Cfg {
 struct Shared {
     uint64_t qfull[2], qempty[2];    // query-strip stages
     uint64_t kfull[2], kempty[2];    // key-slice buffers
-    uint64_t tfull[2], tempty[2];    // TMEM buffers
+    uint64_t tfull[2];               // S of a strip is in TMEM
+    uint64_t eready[2];              // its exponentials are back in TMEM
+    uint64_t tempty[2];              // the TMEM buffer may be written again
     uint64_t xfull[kSlots];          // exchange slots
     uint64_t done;
     uint32_t tmem_base;
     int abort;
     uint64_t wait_ns;
     int wbad[2];                     // 1 + index of the last window (by parity) with a bad block id
+    int unsafe[2];                   // 1 + index of the last window (by parity) whose sums left the safe range
 };
 
 // Exchange slot: the partial (reference, sum) of every CTA for each row.
@@ -109,7 +125,7 @@ size_t smem_bytes()
 {
     using C_ = Cfg<D>;
     const size_t need = 1024 + 2 * (size_t)C_::kKBytes + 2 * (size_t)C_::kQBytes
-                      + (size_t)kSlots * kSlotFloats2 * 8 + 2 * kStrip * 8 + 4 * kSlice * 4 + sizeof(Shared);
+                      + (size_t)kSlots * kSlotFloats2 * 8 + 4 * kSlice * 4 + sizeof(Shared);
     // more than half of the SM's shared memory: a second CTA never shares the
     // SM and waits in tcgen05.alloc for the TMEM this persistent one holds
     const size_t floor_ = 120 * 1024;
@@ -119,7 +135,8 @@ size_t smem_bytes()
 // Bounded wait on an mbarrier phase.  Returns false (without waiting) once the
 // CTA has aborted, or after recording a time-out.
 template <bool CLUSTER = false>
-__device__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *err, bool honour_abort = true)
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *err,
+                                           bool honour_abort = true)
 {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -140,24 +157,12 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *e
 
 __device__ __forceinline__ float fv(uint32_t x) { return __uint_as_float(x); }
 
-// Max of 32 fp32 values (raw bits), a tree of 3-input max of depth 4.
-__device__ __forceinline__ float max32(const uint32_t (&v)[32])
-{
-    float a[11];
-#pragma unroll
-    for (int i = 0; i < 10; ++i) a[i] = max3(fv(v[3 * i]), fv(v[3 * i + 1]), fv(v[3 * i + 2]));
-    a[10] = fmaxf(fv(v[30]), fv(v[31]));
-    const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
-    return max3(max3(b0, b1, b2), a[9], a[10]);
-}
-
-// v[i] <- 2^(v[i]*c2 - r) in place (raw bits) for i in [I0, I0 + 16), z += the
-// values as 4 packed pairs of partial sums.
-template <int I0>
-__device__ __forceinline__ void exp16(uint32_t (&v)[32], uint64_t c2p, uint64_t nrp, uint64_t (&z)[4])
+// v[i] <- 2^(v[i]*c2 - r) in place (raw bits) for the 16 values, z += them as
+// 4 packed pairs of partial sums.
+__device__ __forceinline__ void exp16(uint32_t (&v)[16], uint64_t c2p, uint64_t nrp, uint64_t (&z)[4])
 {
 #pragma unroll
-    for (int i = I0; i < I0 + 16; i += 2) {
+    for (int i = 0; i < 16; i += 2) {
         const uint64_t y = fma2(pack2(fv(v[i]), fv(v[i + 1])), c2p, nrp);
         float y0, y1;
         unpack2(y, y0, y1);
@@ -168,23 +173,85 @@ __device__ __forceinline__ void exp16(uint32_t (&v)[32], uint64_t c2p, uint64_t 
     }
 }
 
-// The softmax side of one CTA for NLD 32-column loads per half row (S = 64*NLD keys).
+// Exponential warps: one per TMEM lane quarter, a thread per query row of the
+// strip and all S = 64 * NLD keys of the slice.
 template <int NLD>
-__device__ __forceinline__ void softmax_role(const Geo &g, Shared *sh, int32_t *err, float *__restrict__ scores,
-                                             uint32_t tmem, const float2 *xs, float2 *hx, float *red, int ncta,
-                                             int T, float c2, int nw, int cid, int nclus, int slice0)
+__device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float2 *xs,
+                                         int ncta, int T, float c2, int nw)
+{
+    constexpr int NCH = 4 * NLD;  // 16-column chunks
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = 32 * warp + lane;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint64_t c2p = pack2(c2, c2);
+    const uint32_t xs_u = smem_u32(xs);
+    float r = 0.f;  // reference of this row position: the previous strip's log2-sum-exp
+    for (int j = 0; j < nw; ++j) {
+        for (int t = 0; t < T; ++t) {
+            const int gt = j * T + t, b = gt & 1, slot = gt & (kSlots - 1);
+            const uint32_t ta = tmem + lane_base + b * 256;
+            wait_phase(smem_u32(&sh->tfull[b]), (gt >> 1) & 1, sh, err);
+            tc_fence_after();
+            uint64_t z4[4] = {0, 0, 0, 0};
+            const uint64_t nrp = pack2(-r, -r);
+            {
+                // two 16-column register sets: chunk c+1 loads while chunk c is
+                // exponentiated (one tcgen05.wait::ld covers all loads in flight)
+                uint32_t ua[16], ub[16];
+                tmem_ld16(ta, ua);
+                tmem_wait_ld16(ua);
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t(&cur)[16] = (c & 1) ? ub : ua;
+                    uint32_t(&nxt)[16] = (c & 1) ? ua : ub;
+                    if (c + 1 < NCH) tmem_ld16(ta + 16 * (c + 1), nxt);
+                    exp16(cur, c2p, nrp, z4);
+                    tmem_st16(ta + 16 * c, cur);
+                    if (c + 1 < NCH) tmem_wait_ld16(nxt);
+                }
+            }
+            float z = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                unpack2(z4[i], lo, hi);
+                z += lo + hi;
+            }
+            // (NaN fails both comparisons and marks the window too)
+            const bool safe = z >= kSumLo && z <= kSumHi;
+            if (!__all_sync(0xffffffffu, safe) && lane == 0) *(volatile int *)&sh->unsafe[j & 1] = j + 1;
+            tmem_wait_st();
+            tc_fence_before();
+            // after a time-out the exchange stops: nothing more is sent
+            if (!*(volatile int *)&sh->abort) {
+                const uint32_t xl = xs_u + 8u * (uint32_t)((slot * kMaxCta + (int)crank) * kStrip + row);
+                const uint32_t xb = smem_u32(&sh->xfull[slot]);
+                for (int c = 0; c < ncta; ++c) st_async_f2(mapa(xl, (uint32_t)c), r, z, mapa(xb, (uint32_t)c));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->eready[b]));
+            if (safe) r += __log2f(z);
+        }
+    }
+}
+
+// Accumulating warps: two per TMEM lane quarter, a thread per query row of the
+// strip and half (NLD 32-column loads) of the slice's keys.
+template <int NLD>
+__device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err, float *__restrict__ scores,
+                                         uint8_t *__restrict__ marks, uint32_t tmem, const float2 *xs, float *red,
+                                         int ncta, int T, int nw, int cid, int nclus, int slice0)
 {
     constexpr int S = 64 * NLD;
     constexpr int HALF = 32 * NLD;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sw = warp - 4, q4 = warp & 3, h = sw >> 2;  // TMEM lane quarter, column half
+    const int aw = warp - 4, q4 = warp & 3, h = aw >> 2;  // TMEM lane quarter, column half
     const int row = 32 * q4 + lane;
-    const int sidx = sw * 32 + lane;
+    const int aidx = aw * 32 + lane;
     const uint32_t crank = cluster_ctarank();
     const int GW = g.G * g.W;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    const uint64_t c2p = pack2(c2, c2);
-    const uint32_t xs_u = smem_u32(xs);
     const uint32_t xbytes = (uint32_t)(ncta * kStrip * 8);  // one slot's bytes from all CTAs
 
     for (int j = 0; j < nw; ++j) {
@@ -195,140 +262,78 @@ __device__ __forceinline__ void softmax_role(const Geo &g, Shared *sh, int32_t *
 #pragma unroll
             for (int p = 0; p < 16; ++p) acc[k][p] = 0;
         for (int t = 0; t < T; ++t) {
-            const int gt = j * T + t, b = gt & 1, slot = gt % kSlots;
+            const int gt = j * T + t, b = gt & 1, slot = gt & (kSlots - 1);
             const uint32_t ta = tmem + lane_base + b * 256 + h * HALF;
-            // ---- phase A: exponentiate this strip's logits once, keep them in TMEM
-            wait_phase(smem_u32(&sh->tfull[b]), (gt >> 1) & 1, sh, err);
+            wait_phase(smem_u32(&sh->eready[b]), (gt >> 1) & 1, sh, err);
             tc_fence_after();
-            float rk[NLD];
-            float r;
-            uint64_t z4[4] = {0, 0, 0, 0};
-            // two register sets: chunk k+1 loads, and its maximum is taken, while
-            // chunk k is exponentiated (one tcgen05.wait::ld covers all loads in flight)
+            // the first two chunks of e come back while the partials are awaited
             uint32_t va[32], vb[32];
             tmem_ld32(ta, va);
-            tmem_wait_ld(va);
-            r = max32(va) * c2 + kMargin;
-            float mn = 0.f;
-#pragma unroll
-            for (int k = 0; k < NLD; ++k) {
-                uint32_t(&cur)[32] = (k & 1) ? vb : va;
-                uint32_t(&nxt)[32] = (k & 1) ? va : vb;
-                if (k > 0) {
-                    if (__any_sync(0xffffffffu, mn > r)) {
-                        // rare: a later chunk exceeds the reference; move it up and rescale the sum
-                        if (mn > r) {
-                            const float rn = mn + kMargin;
-                            const float a = ex2(r - rn);
-                            const uint64_t ap = pack2(a, a);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) z4[i] = fma2(z4[i], ap, 0ull);
-                            r = rn;
-                        }
-                    }
-                }
-                const uint64_t nrp = pack2(-r, -r);
-                if (k + 1 < NLD) tmem_ld32(ta + 32 * (k + 1), nxt);
-                exp16<0>(cur, c2p, nrp, z4);
-                if (k + 1 < NLD) {
-                    tmem_wait_ld_after(nxt, cur);
-                    mn = max32(nxt) * c2;
-                }
-                exp16<16>(cur, c2p, nrp, z4);
-                tmem_st32(ta + 32 * k, cur);
-                rk[k] = r;
-            }
-            float z = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo, hi;
-                unpack2(z4[i], lo, hi);
-                z += lo + hi;
-            }
-            tmem_wait_st();
-            // the first chunk of e comes back while the partials are merged and exchanged
-            tmem_ld32(ta, va);
-            // after a time-out the exchange stops: nothing more is sent and no slot
-            // is armed again, so no barrier sees more arrivals than it expects
-            const bool live = !*(volatile int *)&sh->abort;
-            // the row's two halves merge here; the first half sends the CTA's partial
-            float2 *hrow = hx + (gt & 1) * kStrip + row;
-            if (h == 1) *hrow = make_float2(r, z);
-            named_barrier(2 + q4, 64);
-            if (h == 0 && live) {
-                const float2 o = *hrow;
-                const float rc = fmaxf(r, o.x);
-                const float zc = z * ex2(r - rc) + o.y * ex2(o.x - rc);
-                const uint32_t xl = xs_u + 8u * (uint32_t)((slot * kMaxCta + (int)crank) * kStrip + row);
-                const uint32_t xb = smem_u32(&sh->xfull[slot]);
-                for (int c = 0; c < ncta; ++c) st_async_f2(mapa(xl, (uint32_t)c), rc, zc, mapa(xb, (uint32_t)c));
-            }
-            // ---- phase B: the row's normaliser, then accumulate the weights
-            const bool got = live && wait_phase<true>(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err);
-            float2 pr[kMaxCta];
+            if (NLD > 1) tmem_ld32(ta + 32, vb);
+            const bool got = wait_phase<true>(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err);
             float M = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kMaxCta; ++c)
-                if (c < ncta) {
-                    pr[c] = xs[(slot * kMaxCta + c) * kStrip + row];
-                    M = fmaxf(M, pr[c].x);
-                }
+                if (c < ncta) M = fmaxf(M, xs[(slot * kMaxCta + c) * kStrip + row].x);
             float Z = 0.f;
 #pragma unroll
             for (int c = 0; c < kMaxCta; ++c)
-                if (c < ncta) Z = fmaf(pr[c].y, ex2(pr[c].x - M), Z);
+                if (c < ncta) {
+                    const float2 pc = xs[(slot * kMaxCta + c) * kStrip + row];
+                    Z = fmaf(pc.y, ex2(pc.x - M), Z);
+                }
+            const float rown = xs[(slot * kMaxCta + (int)crank) * kStrip + row].x;
             // rows past G*W (the tail of the last strip) add nothing
-            const float inv = (got && t * kStrip + row < GW) ? rcp_approx(Z) : 0.f;
-            float wk[NLD];
-            bool same = true;
+            const float w = (got && t * kStrip + row < GW) ? rcp_approx(Z) * ex2(rown - M) : 0.f;
+            const uint64_t wp = pack2(w, w);
+            if (NLD > 1) tmem_wait_ld2(va, vb);
+            else tmem_wait_ld(va);
 #pragma unroll
-            for (int k = 0; k < NLD; ++k) same = same && rk[k] == r;
-            if (__all_sync(0xffffffffu, same)) {
-                const float w = inv * ex2(r - M);
+            for (int k = 0; k < NLD; k += 2) {
+                // chunks k, k+1 are in va, vb; k+2, k+3 load into them once consumed
 #pragma unroll
-                for (int k = 0; k < NLD; ++k) wk[k] = w;
-            } else {
+                for (int p = 0; p < 16; ++p) acc[k][p] = fma2(pack2(fv(va[2 * p]), fv(va[2 * p + 1])), wp, acc[k][p]);
+                if (k + 2 < NLD) tmem_ld32(ta + 32 * (k + 2), va);
+                if (k + 1 < NLD) {
 #pragma unroll
-                for (int k = 0; k < NLD; ++k) wk[k] = inv * ex2(rk[k] - M);
-            }
-            tmem_wait_ld(va);
-#pragma unroll
-            for (int k = 0; k < NLD; ++k) {
-                uint32_t(&cur)[32] = (k & 1) ? vb : va;
-                uint32_t(&nxt)[32] = (k & 1) ? va : vb;
-                if (k + 1 < NLD) tmem_ld32(ta + 32 * (k + 1), nxt);
-                const uint64_t wp = pack2(wk[k], wk[k]);
-#pragma unroll
-                for (int p = 0; p < 16; ++p) acc[k][p] = fma2(pack2(fv(cur[2 * p]), fv(cur[2 * p + 1])), wp, acc[k][p]);
-                if (k + 1 < NLD) tmem_wait_ld(nxt);
+                    for (int p = 0; p < 16; ++p)
+                        acc[k + 1][p] = fma2(pack2(fv(vb[2 * p]), fv(vb[2 * p + 1])), wp, acc[k + 1][p]);
+                    if (k + 3 < NLD) tmem_ld32(ta + 32 * (k + 3), vb);
+                }
+                if (k + 3 < NLD) tmem_wait_ld2(va, vb);
+                else if (k + 2 < NLD) tmem_wait_ld(va);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
             // the slot's next use is strip gt + kSlots; every peer sends it only after
-            // this CTA has finished this strip (see the slot count)
-            if (sidx == 0 && got) mbar_arrive_expect_tx(smem_u32(&sh->xfull[slot]), xbytes);
+            // this CTA has released the buffer of strip gt + kSlots - 2
+            if (aidx == 0 && got) mbar_arrive_expect_tx(smem_u32(&sh->xfull[slot]), xbytes);
         }
 
-        // ---- window done: column sums over the 128 lanes, in a fixed order
-        float vals[NLD * 32];
+        // ---- window done: column sums over the 128 lanes, in a fixed order.
+        // One 32-key chunk at a time: a butterfly over the warp's lanes (after the
+        // round with offset o a lane keeps the half of its range selected by bit o
+        // of its lane id) leaves lane l with key 32k + l summed over the warp's 32
+        // rows; the four lane quarters are added through shared memory below.
+        named_barrier(1, kAcc);  // the previous window's sums have been read
 #pragma unroll
-        for (int k = 0; k < NLD; ++k)
+        for (int k = 0; k < NLD; ++k) {
+            float vals[32];
 #pragma unroll
-            for (int p = 0; p < 16; ++p) unpack2(acc[k][p], vals[32 * k + 2 * p], vals[32 * k + 2 * p + 1]);
-        // butterfly over the warp's lanes: after the round with offset o the lane
-        // keeps the half of its range selected by bit o of its lane id
+            for (int p = 0; p < 16; ++p) unpack2(acc[k][p], vals[2 * p], vals[2 * p + 1]);
 #pragma unroll
-        for (int o = 16, n = NLD * 32; o >= 1; o >>= 1, n >>= 1) {
-            const bool upper = (lane & o) != 0;
+            for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+                const bool upper = (lane & o) != 0;
 #pragma unroll
-            for (int i = 0; i < n / 2; ++i) {
-                const float send = upper ? vals[i] : vals[n / 2 + i];
-                const float keep = upper ? vals[n / 2 + i] : vals[i];
-                vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                for (int i = 0; i < n / 2; ++i) {
+                    const float send = upper ? vals[i] : vals[n / 2 + i];
+                    const float keep = upper ? vals[n / 2 + i] : vals[i];
+                    vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
             }
+            red[q4 * kSlice + h * HALF + 32 * k + lane] = vals[0];
         }
-        // lane l now holds keys NLD*l .. NLD*l + NLD - 1 of its half, summed over its warp's 32 rows.
         // The window's validity, from the same table the producer read (a window
         // with a bad block id or length was not loaded; its scores are zeros).
         int ws_, wl_, wh_;
@@ -336,30 +341,31 @@ __device__ __forceinline__ void softmax_role(const Geo &g, Shared *sh, int32_t *
         const int32_t L = g.len[ws_];
         const bool len_ok = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
         if (len_ok) {
-            const int lb = (L - g.W) / g.bs + sidx;  // at most W/16 + 1 <= 65 blocks per window
+            const int lb = (L - g.W) / g.bs + aidx;  // at most W/16 + 1 <= 65 blocks per window
             if (lb < (L + g.bs - 1) / g.bs) {
                 const int32_t bid = g.bt[(int64_t)ws_ * g.bt_stride + lb];
                 if (bid < 0 || bid >= g.num_blocks) sh->wbad[j & 1] = j + 1;
             }
         }
-        named_barrier(1, kSoft);
+        named_barrier(1, kAcc);
         const int stat = !len_ok ? KARA_EINVAL : *(volatile int *)&sh->wbad[j & 1] == j + 1 ? KARA_EBADBLOCK : 0;
-#pragma unroll
-        for (int k = 0; k < NLD; ++k) red[q4 * kSlice + h * HALF + NLD * lane + k] = vals[k];
-        named_barrier(1, kSoft);
-        if (sidx < S) {
-            const float sum = ((red[sidx] + red[kSlice + sidx]) + red[2 * kSlice + sidx]) + red[3 * kSlice + sidx];
-            const int key = slice0 + sidx;
+        if (aidx < S) {
+            const float sum = ((red[aidx] + red[kSlice + aidx]) + red[2 * kSlice + aidx]) + red[3 * kSlice + aidx];
+            const int key = slice0 + aidx;
             if (key < g.C) scores[u * g.C + key] = stat ? 0.f : sum;
         }
-        if (stat && sidx == 0) set_err(err, stat);
+        if (stat && aidx == 0) set_err(err, stat);
+        // the exponential warps marked this window (in this CTA) if a sum left the
+        // safe range; the exact kernel recomputes marked windows
+        if (aidx == 0 && !stat && *(volatile int *)&sh->unsafe[j & 1] == j + 1) marks[u] = 1;
     }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     score_sp_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, const Geo g,
-                    float *__restrict__ scores, int32_t *err, int ncta, int T, float c2, uint64_t wait_ns, int stall)
+                    float *__restrict__ scores, uint8_t *__restrict__ marks, int32_t *err, int ncta, int T, float c2,
+                    uint64_t wait_ns, int stall)
 {
     using C_ = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -368,8 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sK = base;                                   // two key buffers
     uint8_t *sQ = sK + 2 * C_::kKBytes;                   // two query stages
     float2 *xs = reinterpret_cast<float2 *>(sQ + 2 * C_::kQBytes);
-    float2 *hx = xs + kSlots * kSlotFloats2;              // the halves' partials, by strip parity
-    float *red = reinterpret_cast<float *>(hx + 2 * kStrip);
+    float *red = reinterpret_cast<float *>(xs + kSlots * kSlotFloats2);
     Shared *sh = reinterpret_cast<Shared *>(red + 4 * kSlice);
     const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
 
@@ -385,24 +390,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh->abort = 0;
         sh->wait_ns = wait_ns;
         sh->wbad[0] = sh->wbad[1] = 0;
+        sh->unsafe[0] = sh->unsafe[1] = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sh->qfull[i]), 1);
             mbar_init(smem_u32(&sh->qempty[i]), 1);
             mbar_init(smem_u32(&sh->kfull[i]), 1);
             mbar_init(smem_u32(&sh->kempty[i]), 1);
             mbar_init(smem_u32(&sh->tfull[i]), 1);
-            mbar_init(smem_u32(&sh->tempty[i]), kSoft / 32);
+            mbar_init(smem_u32(&sh->eready[i]), 4);
+            mbar_init(smem_u32(&sh->tempty[i]), kAcc / 32);
         }
         for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&sh->xfull[i]), 1);
         mbar_init(smem_u32(&sh->done), 1);
         fence_mbarrier_init();
         for (int i = 0; i < kSlots; ++i) mbar_arrive_expect_tx(smem_u32(&sh->xfull[i]), (uint32_t)(ncta * kStrip * 8));
     }
-    if (warp == 1) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         prefetch_tmap(&qmap);
         prefetch_tmap(&kmap);
     }
@@ -413,29 +420,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_arrive();
     cluster_wait();
     const uint32_t tmem = sh->tmem_base;
+    const int nld = S / 64;
 
-    if (warp >= 4) {
-        // ---------------- softmax warpgroups ---------------------------------
-        // (the register increase sits in the same branch as the code that uses it)
-        reg_alloc<kRegsHigh>();
-        const int nld = S / 64;
+    // (each warpgroup's register change sits in the same branch as the code that uses it)
+    if (warp < 4) {
+        // ---------------- exponentials --------------------------------------
+        reg_dealloc<kRegsExp>();
         if (nld == 4)
-            softmax_role<4>(g, sh, err, scores, tmem, xs, hx, red, ncta, T, c2, nw, cid, nclus, slice0);
+            exp_role<4>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else if (nld == 3)
-            softmax_role<3>(g, sh, err, scores, tmem, xs, hx, red, ncta, T, c2, nw, cid, nclus, slice0);
+            exp_role<3>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else if (nld == 2)
-            softmax_role<2>(g, sh, err, scores, tmem, xs, hx, red, ncta, T, c2, nw, cid, nclus, slice0);
+            exp_role<2>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else
-            softmax_role<1>(g, sh, err, scores, tmem, xs, hx, red, ncta, T, c2, nw, cid, nclus, slice0);
+            exp_role<1>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+    } else if (warp < 12) {
+        // ---------------- accumulation ---------------------------------------
+        reg_alloc<kRegsAcc>();
+        if (nld == 4)
+            acc_role<4>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+        else if (nld == 3)
+            acc_role<3>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+        else if (nld == 2)
+            acc_role<2>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+        else
+            acc_role<1>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
     } else {
-        reg_dealloc<kRegsLow>();
-        if (warp == 0) {
+        reg_dealloc<kRegsCtl>();
+        if (warp == 12) {
             // ---------------- producer: key slices and query strips by TMA --------
             int issued = 0, kissued = 0;  // query strips, key slices issued
             // Window j's key slice goes into buffer j & 1, one TMA box per (paged
             // block, 64-column atom), a block's 16 rows at 16-row steps; a block
             // id outside the pool reads zeros (the tensor map's bounds) and the
-            // softmax warps report the window.
+            // accumulating warps report the window.
             auto load_k = [&](int j) {
                 const int64_t u = cid + (int64_t)j * nclus;
                 int s, l, h;
@@ -499,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_phase(smem_u32(&sh->kfull[j & 1]), (j >> 1) & 1, sh, err, false);
             }
             __syncwarp();
-        } else if (warp == 1) {
+        } else if (warp == 13) {
             // ---------------- MMA issuer -----------------------------------------
             const uint32_t idesc = idesc_bf16(128, S);
             if (lane == 0) {
@@ -545,14 +563,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no CTA leaves while a peer may still send to its shared memory
     cluster_arrive();
     cluster_wait();
-    if (warp == 1) {
+    if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
+// Exact scores of the marked windows on the CUDA cores (fp32; the row maximum
+// found before any exponential): each CTA walks the marks of its share of the
+// windows and computes the few marked ones.  Unmarked windows cost one byte read.
+constexpr int kFbThreads = 256;
+constexpr int kFbMaxGW = 8192;
+
+__global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *__restrict__ scores,
+                                                           const uint8_t *__restrict__ marks)
+{
+    __shared__ float lse[kFbMaxGW];
+    const float sc = 1.f / sqrtf((float)g.D);
+    for (int64_t u = blockIdx.x; u < g.nwin; u += gridDim.x) {
+        if (!marks[u]) continue;
+        int s, l, h;
+        window_coords(g, u, s, l, h);
+        const int32_t L = g.len[s];
+        const int ws = L - g.W, GW = g.G * g.W;
+        const int32_t *btr = g.bt + (int64_t)s * g.bt_stride;
+        const uint16_t *qw = g.q + (((int64_t)s * g.layers + l) * g.hq + (int64_t)h * g.G) * g.W * g.D;
+        auto key = [&](int j) { const int x = ws + j; return g.k + pool_off(g, l, btr[x / g.bs], h, x % g.bs); };
+        auto bf = [](uint16_t x) { return __uint_as_float((uint32_t)x << 16); };
+        auto dot = [&](const uint16_t *a, const uint16_t *b) {
+            float acc = 0.f;
+            for (int d = 0; d < g.D; ++d) acc = fmaf(bf(a[d]), bf(b[d]), acc);
+            return acc * sc;
+        };
+        // pass 1: per query row, log-sum-exp over all W keys (maximum first)
+        for (int r = threadIdx.x; r < GW; r += blockDim.x) {
+            const uint16_t *q = qw + (int64_t)r * g.D;
+            float m = -INFINITY;
+            for (int j = 0; j < g.W; ++j) m = fmaxf(m, dot(q, key(j)));
+            float z = 0.f;
+            for (int j = 0; j < g.W; ++j) z += expf(dot(q, key(j)) - m);
+            lse[r] = m + logf(z);
+        }
+        __syncthreads();
+        // pass 2: per compressible key, the sum of the rows' probabilities
+        for (int j = threadIdx.x; j < g.C; j += blockDim.x) {
+            const uint16_t *k = key(j);
+            float acc = 0.f;
+            for (int r = 0; r < GW; ++r) acc += expf(dot(qw + (int64_t)r * g.D, k) - lse[r]);
+            scores[u * g.C + j] = acc;
+        }
+        __syncthreads();
+    }
+}
+
 template <int D>
-cudaError_t launch_sp(const Geo &g, float *scores, int32_t *err, cudaStream_t st)
+cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err, cudaStream_t st)
 {
     const int ncta = (g.W + kSlice - 1) / kSlice;
     const int T = (g.G * g.W + kStrip - 1) / kStrip;
@@ -626,17 +691,27 @@ cudaError_t launch_sp(const Geo &g, float *scores, int32_t *err, cudaStream_t st
     cfg.gridDim = dim3((unsigned)(nclus * ncta));
     const float c2 = 1.4426950408889634f / sqrtf((float)D);
     const Stall dbg = debug_stall(kTimeoutNs);
-    return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, g, scores, err, ncta, T, c2, dbg.wait_ns, (int)dbg.on);
+    e = cudaMemsetAsync(marks, 0, (size_t)g.nwin, st);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, kern, qmap, kmap, g, scores, marks, err, ncta, T, c2, dbg.wait_ns, (int)dbg.on);
+    if (e != cudaSuccess) return e;
+    const unsigned fb_blocks = (unsigned)(g.nwin < 1184 ? g.nwin : 1184);
+    exact_kernel<<<fb_blocks, kFbThreads, 0, st>>>(g, scores, marks);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 // The single-pass kernel covers bidirectional scoring with at most kMaxCta key slices.
-bool score_sp_supported(const Geo &g) { return !g.causal && g.W <= kSlice * kMaxCta; }
+bool score_sp_supported(const Geo &g) { return !g.causal && g.W <= kSlice * kMaxCta && g.G * g.W <= kFbMaxGW; }
 
-cudaError_t launch_score_sp(const Geo &g, float *scores, int32_t *err, cudaStream_t st)
+// Scratch of the single-pass path: one mark byte per window.
+size_t score_sp_scratch_bytes(const Geo &g) { return g.W <= kSlice * kMaxCta ? align256((size_t)g.nwin) : 0; }
+
+cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
 {
-    return g.D == 128 ? launch_sp<128>(g, scores, err, st) : launch_sp<64>(g, scores, err, st);
+    uint8_t *marks = static_cast<uint8_t *>(scratch);
+    return g.D == 128 ? launch_sp<128>(g, scores, marks, err, st) : launch_sp<64>(g, scores, marks, err, st);
 }
 
 }  // namespace kara

@@ -652,17 +652,20 @@ cudaError_t launch_tc(const Geo &g, float *scores, int32_t *err, cudaStream_t st
 
 }  // namespace
 
-size_t score_scratch_bytes(const Geo &) { return 0; }
+size_t score_sp_scratch_bytes(const Geo &g);
+
+// Scratch of the scoring path (the single-pass kernel's per-window marks).
+size_t score_scratch_bytes(const Geo &g) { return score_sp_scratch_bytes(g); }
 
 bool score_sp_supported(const Geo &g);
-cudaError_t launch_score_sp(const Geo &g, float *scores, int32_t *err, cudaStream_t st);
+cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
 
-cudaError_t launch_score(const Geo &g, float *scores, void *, int32_t *err, cudaStream_t st)
+cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
 {
     if (g.nwin == 0) return cudaSuccess;
     // one pass over the logits where the single-pass kernel covers the shape;
     // the two-pass kernel for the causal ablation and windows above 1024 keys
-    if (score_sp_supported(g)) return launch_score_sp(g, scores, err, st);
+    if (score_sp_supported(g)) return launch_score_sp(g, scores, scratch, err, st);
     if (g.G * g.W > 8192) return cudaErrorInvalidValue;
     return g.D == 128 ? launch_tc<128>(g, scores, err, st) : launch_tc<64>(g, scores, err, st);
 }
