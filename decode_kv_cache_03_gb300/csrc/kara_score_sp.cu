@@ -134,13 +134,17 @@ size_t smem_bytes()
 
 // Bounded wait on an mbarrier phase.  Returns false (without waiting) once the
 // CTA has aborted, or after recording a time-out.
-template <bool CLUSTER = false>
+// POLL: test without suspending (for the MMA issuer, whose reaction is on the
+// critical path).
+template <bool CLUSTER = false, bool POLL = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Shared *sh, int32_t *err,
                                            bool honour_abort = true)
 {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (CLUSTER ? mbar_try_wait_cluster(bar, parity)
+                    : POLL ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
+            return true;
         if ((it & 255u) == 255u) {
             if (honour_abort && *(volatile int *)&sh->abort) return false;
             const uint64_t now = globaltimer();
@@ -270,21 +274,28 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
             uint32_t va[32], vb[32];
             tmem_ld32(ta, va);
             if (NLD > 1) tmem_ld32(ta + 32, vb);
-            const bool got = wait_phase<true>(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err);
+            // (the complete-tx of the partials' st.async makes them visible to the
+            // threads that see the phase complete)
+            const bool got = wait_phase(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err);
+            float2 pr[kMaxCta];
             float M = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kMaxCta; ++c)
-                if (c < ncta) M = fmaxf(M, xs[(slot * kMaxCta + c) * kStrip + row].x);
-            float Z = 0.f;
+                if (c < ncta) {
+                    pr[c] = xs[(slot * kMaxCta + c) * kStrip + row];
+                    M = fmaxf(M, pr[c].x);
+                }
+            // the combine's exponentials on the FMA pipe: the special-function unit
+            // is the exponential warps'
+            float Z = 0.f, rown = 0.f;
 #pragma unroll
             for (int c = 0; c < kMaxCta; ++c)
                 if (c < ncta) {
-                    const float2 pc = xs[(slot * kMaxCta + c) * kStrip + row];
-                    Z = fmaf(pc.y, ex2(pc.x - M), Z);
+                    Z = fmaf(pr[c].y, exp2_poly(pr[c].x - M), Z);
+                    if (c == (int)crank) rown = pr[c].x;
                 }
-            const float rown = xs[(slot * kMaxCta + (int)crank) * kStrip + row].x;
             // rows past G*W (the tail of the last strip) add nothing
-            const float w = (got && t * kStrip + row < GW) ? rcp_approx(Z) * ex2(rown - M) : 0.f;
+            const float w = (got && t * kStrip + row < GW) ? __fdividef(exp2_poly(rown - M), Z) : 0.f;
             const uint64_t wp = pack2(w, w);
             if (NLD > 1) tmem_wait_ld2(va, vb);
             else tmem_wait_ld(va);
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < T && ok; ++t) {
                         const int gt = j * T + t, st = gt & 1;
                         ok = wait_phase(smem_u32(&sh->qfull[st]), (gt >> 1) & 1, sh, err) &&
-                             wait_phase(smem_u32(&sh->tempty[st]), ((gt >> 1) & 1) ^ 1, sh, err);
+                             wait_phase<false, true>(smem_u32(&sh->tempty[st]), ((gt >> 1) & 1) ^ 1, sh, err);
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll

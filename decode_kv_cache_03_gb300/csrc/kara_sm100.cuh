@@ -55,6 +55,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of an mbarrier phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ---- TMA --------------------------------------------------------------------
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
@@ -386,7 +398,9 @@ __device__ __forceinline__ float max3(float a, float b, float c)
 // 3e-6.  2^n is applied by adding n to the exponent field.  Inputs are clamped
 // at -126 so the exponent never underflows (2^-126 stands in for anything
 // smaller, as the flush-to-zero ex2 gives 0 there).  An FMA-pipe alternative
-// to ex2; the scoring kernel measured it slower and does not call it.
+// to ex2, for the few exponentials of the single-pass scorer's accumulating
+// warps, which would otherwise queue behind the exponential warps' stream on
+// the special-function unit.
 constexpr float kExp2C0 = 0.99999928474426270f;
 constexpr float kExp2C1 = 0.69312179088592530f;
 constexpr float kExp2C2 = 0.24024744331836700f;
@@ -411,6 +425,14 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t y2)
     const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
     const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
     return pack2(r0, r1);
+}
+
+// Scalar form of exp2_poly2 (same coefficients and steps).
+__device__ __forceinline__ float exp2_poly(float y)
+{
+    float lo, hi;
+    unpack2(exp2_poly2(pack2(y, y)), lo, hi);
+    return lo;
 }
 
 }  // namespace ptx
