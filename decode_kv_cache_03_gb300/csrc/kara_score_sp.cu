@@ -24,21 +24,23 @@
 //   * Exponential warps (one per TMEM lane quarter; a thread owns one query row
 //     and all of the slice's keys) turn the strip's logits into
 //     e = 2^(l2 - r), l2 = <q,k> log2(e)/sqrt(D), written back over S in TMEM,
-//     and send the CTA's partial (r, z = sum e) of the row to every CTA of the
+//     and send the CTA's partial sum z = sum e of the row to every CTA of the
 //     cluster with st.async (DSMEM, completing bytes on the receiver's
-//     mbarrier).  The reference r is the row position's log-sum-exp from the
-//     previous strip, so no pass over the logits precedes the exponentials.
-//     A strip whose sum leaves [2^-88, 2^119] -- where the fp32 exponentials
-//     could overflow, or lose terms within 2^-30 of the row maximum -- marks
-//     its window, and an exact CUDA-core kernel recomputes marked windows
-//     afterwards (with the usual logit ranges no window is marked).
+//     mbarrier).  The reference r is common to the cluster: the row position's
+//     log-sum-exp two strips earlier, r + log2(sum_c z_c), which every CTA
+//     derives from the same exchanged partials in the same order (two strips
+//     back, that exchange has long completed).  So no pass over the logits
+//     precedes the exponentials, and the row's normaliser is a plain sum.  A strip whose row total sum_c z_c leaves [2^-88, 2^119] --
+//     where the fp32 exponentials could overflow, or lose terms within 2^-30
+//     of the row maximum -- marks its window, and an exact CUDA-core kernel
+//     recomputes marked windows afterwards (with the usual logit ranges no
+//     window is marked).
 //   * Accumulating warps (two per lane quarter, half of the keys each) wait
-//     for the ncta partials of their row, form the row's normaliser
-//     Z = sum_c z_c 2^(r_c - M) exactly, read e back from TMEM and accumulate
-//     e * 2^(r - M) / Z in registers, one fp32 accumulator per (row lane,
-//     key).  That releases the TMEM buffer for the next strip's MMA.  The
-//     exponential warps never wait for the exchange, so the exponentials of
-//     one strip overlap the exchange and accumulation of the previous one.
+//     for the ncta partials of their row, form Z = sum_c z_c in a fixed order,
+//     read e back from TMEM and accumulate e / Z in registers, one fp32
+//     accumulator per (row lane, key).  That releases the TMEM buffer for the
+//     next strip's MMA.  The exponentials of one strip overlap the exchange
+//     and accumulation of the previous one.
 //   * After a window's last strip the accumulators are summed across the 32
 //     lanes of each warp (a butterfly that leaves each lane whole keys) and
 //     across the four lane quarters through shared memory, in a fixed order.
@@ -47,9 +49,11 @@
 // the next window's key slice loads into the second key buffer while the
 // current window is scored.  No W x W matrix and no per-row statistic reaches
 // global memory; every score is a deterministic fp32 sum.  Warp roles (512
-// threads): warps 0..3 exponentials, 4..11 accumulation, 12 TMA, 13 TMEM
-// allocation and MMAs (one lane), 14..15 idle; the warpgroups trade registers
-// so the accumulating warps hold 128 accumulators each.  Every wait is bounded;
+// threads): warps 0..3 exponentials, 4..11 accumulation, 12 query-strip TMA,
+// 13 TMEM allocation and MMAs (one lane), 14 key-slice TMA (it also reads the
+// window's length and block ids once and publishes the first key's row offset
+// and the window's validity in shared memory), 15 idle; the warpgroups trade
+// registers so the accumulating warps hold 128 accumulators each.  Every wait is bounded;
 // on time-out the CTA records KARA_ETIMEOUT and stops waiting, still draining
 // what it has in flight.
 #include <cuda.h>
@@ -78,14 +82,18 @@ constexpr int kThreads = 512;  // warpgroups: exponentials, accumulation x2, TMA
 // add up: 128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch.
 constexpr int kRegsLaunch = 128;
 constexpr uint32_t kRegsExp = 72;
-constexpr uint32_t kRegsAcc = 208;
-constexpr uint32_t kRegsCtl = 24;
+constexpr uint32_t kRegsAcc = 192;
+constexpr uint32_t kRegsCtl = 56;
 static_assert(128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch, "register trade must add up");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr uint64_t kDrainNs = 20000ull;  // landing time allowed to DSMEM stores after a time-out
 constexpr int kBlockRows = 16;                         // rows of a paged block
 constexpr int kSliceBlocks = kSlice / kBlockRows + 1;  // blocks a slice can touch (17)
 constexpr int kKAtomBytes = kSliceBlocks * kBlockRows * 128;  // one 64-column atom of a key buffer
+// Window statuses in flight: window j + kWinRing is loaded only after the
+// accumulating warps have finished window j, even with one strip per window.
+constexpr int kWinRing = 8;
 // A row's sum of exponentials relative to its reference must lie here for the
 // fp32 exponentials to be exact to rounding: above, the largest could
 // overflow; below, terms within 2^-30 of the row maximum could flush to zero.
@@ -109,23 +117,25 @@ struct Shared {
     uint64_t eready[2];              // its exponentials are back in TMEM
     uint64_t tempty[2];              // the TMEM buffer may be written again
     uint64_t xfull[kSlots];          // exchange slots
+    uint64_t wfull[kWinRing];        // a window's status is published
     uint64_t done;
     uint32_t tmem_base;
     int abort;
     uint64_t wait_ns;
-    int wbad[2];                     // 1 + index of the last window (by parity) with a bad block id
     int unsafe[2];                   // 1 + index of the last window (by parity) whose sums left the safe range
+    int koff[2];                     // row of the window's first key in each key buffer
+    int wstat[kWinRing];             // a window's status: 0, KARA_EINVAL or KARA_EBADBLOCK
 };
 
-// Exchange slot: the partial (reference, sum) of every CTA for each row.
-constexpr int kSlotFloats2 = kMaxCta * kStrip;
+// Exchange slot: the partial sum of every CTA for each row.
+constexpr int kSlotFloats = kMaxCta * kStrip;
 
 template <int D>
 size_t smem_bytes()
 {
     using C_ = Cfg<D>;
     const size_t need = 1024 + 2 * (size_t)C_::kKBytes + 2 * (size_t)C_::kQBytes
-                      + (size_t)kSlots * kSlotFloats2 * 8 + 4 * kSlice * 4 + sizeof(Shared);
+                      + (size_t)kSlots * kSlotFloats * 4 + 4 * kSlice * 4 + sizeof(Shared);
     // more than half of the SM's shared memory: a second CTA never shares the
     // SM and waits in tcgen05.alloc for the TMEM this persistent one holds
     const size_t floor_ = 120 * 1024;
@@ -161,6 +171,19 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Shared
 
 __device__ __forceinline__ float fv(uint32_t x) { return __uint_as_float(x); }
 
+// Row total of an exchange slot: the CTAs' partial sums added in CTA order, so
+// every CTA of the cluster (and both warp roles) gets the same value.
+__device__ __forceinline__ float slot_total(const float *xs, int slot, int ncta, int row)
+{
+    float Z = xs[slot * kSlotFloats + row];
+#pragma unroll
+    for (int c = 1; c < kMaxCta; ++c)
+        if (c < ncta) Z += xs[slot * kSlotFloats + c * kStrip + row];
+    return Z;
+}
+
+__device__ __forceinline__ bool in_safe_range(float Z) { return Z >= kSumLo && Z <= kSumHi; }  // NaN: false
+
 // v[i] <- 2^(v[i]*c2 - r) in place (raw bits) for the 16 values, z += them as
 // 4 packed pairs of partial sums.
 __device__ __forceinline__ void exp16(uint32_t (&v)[16], uint64_t c2p, uint64_t nrp, uint64_t (&z)[4])
@@ -180,7 +203,7 @@ __device__ __forceinline__ void exp16(uint32_t (&v)[16], uint64_t c2p, uint64_t 
 // Exponential warps: one per TMEM lane quarter, a thread per query row of the
 // strip and all S = 64 * NLD keys of the slice.
 template <int NLD>
-__device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float2 *xs,
+__device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float *xs,
                                          int ncta, int T, float c2, int nw)
 {
     constexpr int NCH = 4 * NLD;  // 16-column chunks
@@ -190,12 +213,28 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const uint64_t c2p = pack2(c2, c2);
     const uint32_t xs_u = smem_u32(xs);
-    float r = 0.f;  // reference of this row position: the previous strip's log2-sum-exp
+    // references of this row position for even and odd strips, the same in every
+    // CTA of the cluster
+    float rr[2] = {0.f, 0.f};
     for (int j = 0; j < nw; ++j) {
         for (int t = 0; t < T; ++t) {
             const int gt = j * T + t, b = gt & 1, slot = gt & (kSlots - 1);
+            // the row total of strip gt - 2 moves that strip's reference to the
+            // row's log2-sum-exp (an out-of-range total, which marks its window,
+            // or a missing one after a time-out leaves it where it was; once the
+            // CTA has aborted, the slots' phases no longer follow the strips)
+            if (gt > 1) {
+                const int ps = (gt - 2) & (kSlots - 1);
+                if (wait_phase(smem_u32(&sh->xfull[ps]), (uint32_t)((gt - 2) / kSlots) & 1u, sh, err) &&
+                    !*(volatile int *)&sh->abort) {
+                    const float Z = slot_total(xs, ps, ncta, row);
+                    if (in_safe_range(Z)) rr[b] += __log2f(Z);
+                }
+            }
+            const float r = rr[b];
             const uint32_t ta = tmem + lane_base + b * 256;
             wait_phase(smem_u32(&sh->tfull[b]), (gt >> 1) & 1, sh, err);
+            __syncwarp();  // the TMEM accesses below are warp-collective
             tc_fence_after();
             uint64_t z4[4] = {0, 0, 0, 0};
             const uint64_t nrp = pack2(-r, -r);
@@ -222,20 +261,16 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                 unpack2(z4[i], lo, hi);
                 z += lo + hi;
             }
-            // (NaN fails both comparisons and marks the window too)
-            const bool safe = z >= kSumLo && z <= kSumHi;
-            if (!__all_sync(0xffffffffu, safe) && lane == 0) *(volatile int *)&sh->unsafe[j & 1] = j + 1;
             tmem_wait_st();
             tc_fence_before();
             // after a time-out the exchange stops: nothing more is sent
             if (!*(volatile int *)&sh->abort) {
-                const uint32_t xl = xs_u + 8u * (uint32_t)((slot * kMaxCta + (int)crank) * kStrip + row);
+                const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotFloats + (int)crank * kStrip + row);
                 const uint32_t xb = smem_u32(&sh->xfull[slot]);
-                for (int c = 0; c < ncta; ++c) st_async_f2(mapa(xl, (uint32_t)c), r, z, mapa(xb, (uint32_t)c));
+                for (int c = 0; c < ncta; ++c) st_async_f32(mapa(xl, (uint32_t)c), z, mapa(xb, (uint32_t)c));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->eready[b]));
-            if (safe) r += __log2f(z);
         }
     }
 }
@@ -244,75 +279,63 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
 // strip and half (NLD 32-column loads) of the slice's keys.
 template <int NLD>
 __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err, float *__restrict__ scores,
-                                         uint8_t *__restrict__ marks, uint32_t tmem, const float2 *xs, float *red,
+                                         uint8_t *__restrict__ marks, uint32_t tmem, const float *xs, float *red,
                                          int ncta, int T, int nw, int cid, int nclus, int slice0)
 {
     constexpr int S = 64 * NLD;
     constexpr int HALF = 32 * NLD;
+    constexpr int NC = 2 * NLD;  // 16-column chunks of this thread's half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int aw = warp - 4, q4 = warp & 3, h = aw >> 2;  // TMEM lane quarter, column half
     const int row = 32 * q4 + lane;
     const int aidx = aw * 32 + lane;
-    const uint32_t crank = cluster_ctarank();
     const int GW = g.G * g.W;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    const uint32_t xbytes = (uint32_t)(ncta * kStrip * 8);  // one slot's bytes from all CTAs
+    const uint32_t xbytes = (uint32_t)(ncta * kStrip * 4);  // one slot's bytes from all CTAs
 
     for (int j = 0; j < nw; ++j) {
         const int64_t u = cid + (int64_t)j * nclus;
-        uint64_t acc[NLD][16];
+        uint64_t acc[NC][8];
 #pragma unroll
-        for (int k = 0; k < NLD; ++k)
+        for (int k = 0; k < NC; ++k)
 #pragma unroll
-            for (int p = 0; p < 16; ++p) acc[k][p] = 0;
+            for (int p = 0; p < 8; ++p) acc[k][p] = 0;
         for (int t = 0; t < T; ++t) {
             const int gt = j * T + t, b = gt & 1, slot = gt & (kSlots - 1);
             const uint32_t ta = tmem + lane_base + b * 256 + h * HALF;
             wait_phase(smem_u32(&sh->eready[b]), (gt >> 1) & 1, sh, err);
+            __syncwarp();  // the TMEM accesses below are warp-collective
             tc_fence_after();
             // the first two chunks of e come back while the partials are awaited
-            uint32_t va[32], vb[32];
-            tmem_ld32(ta, va);
-            if (NLD > 1) tmem_ld32(ta + 32, vb);
+            uint32_t va[16], vb[16];
+            tmem_ld16(ta, va);
+            tmem_ld16(ta + 16, vb);
             // (the complete-tx of the partials' st.async makes them visible to the
-            // threads that see the phase complete)
-            const bool got = wait_phase(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err);
-            float2 pr[kMaxCta];
-            float M = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kMaxCta; ++c)
-                if (c < ncta) {
-                    pr[c] = xs[(slot * kMaxCta + c) * kStrip + row];
-                    M = fmaxf(M, pr[c].x);
-                }
-            // the combine's exponentials on the FMA pipe: the special-function unit
-            // is the exponential warps'
-            float Z = 0.f, rown = 0.f;
-#pragma unroll
-            for (int c = 0; c < kMaxCta; ++c)
-                if (c < ncta) {
-                    Z = fmaf(pr[c].y, exp2_poly(pr[c].x - M), Z);
-                    if (c == (int)crank) rown = pr[c].x;
-                }
-            // rows past G*W (the tail of the last strip) add nothing
-            const float w = (got && t * kStrip + row < GW) ? __fdividef(exp2_poly(rown - M), Z) : 0.f;
+            // threads that see the phase complete).  Once the CTA has aborted, a
+            // slot's phase parity no longer tells which strip it belongs to: the
+            // partials are not used and the slot is not armed again (an extra
+            // arrival on a barrier whose phase is still pending would over-arrive).
+            const bool got = wait_phase(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err) &&
+                             !*(volatile int *)&sh->abort;
+            const float Z = slot_total(xs, slot, ncta, row);
+            // rows past G*W (the tail of the last strip) add nothing; a row total
+            // out of the safe range marks the window for the exact recompute
+            const bool live = got && t * kStrip + row < GW;
+            if (live && !in_safe_range(Z)) *(volatile int *)&sh->unsafe[j & 1] = j + 1;
+            const float w = (live && in_safe_range(Z)) ? rcp_approx(Z) : 0.f;
             const uint64_t wp = pack2(w, w);
-            if (NLD > 1) tmem_wait_ld2(va, vb);
-            else tmem_wait_ld(va);
+            tmem_wait_ld16x2(va, vb);
 #pragma unroll
-            for (int k = 0; k < NLD; k += 2) {
+            for (int k = 0; k < NC; k += 2) {
                 // chunks k, k+1 are in va, vb; k+2, k+3 load into them once consumed
 #pragma unroll
-                for (int p = 0; p < 16; ++p) acc[k][p] = fma2(pack2(fv(va[2 * p]), fv(va[2 * p + 1])), wp, acc[k][p]);
-                if (k + 2 < NLD) tmem_ld32(ta + 32 * (k + 2), va);
-                if (k + 1 < NLD) {
+                for (int p = 0; p < 8; ++p) acc[k][p] = fma2(pack2(fv(va[2 * p]), fv(va[2 * p + 1])), wp, acc[k][p]);
+                if (k + 2 < NC) tmem_ld16(ta + 16 * (k + 2), va);
 #pragma unroll
-                    for (int p = 0; p < 16; ++p)
-                        acc[k + 1][p] = fma2(pack2(fv(vb[2 * p]), fv(vb[2 * p + 1])), wp, acc[k + 1][p]);
-                    if (k + 3 < NLD) tmem_ld32(ta + 32 * (k + 3), vb);
-                }
-                if (k + 3 < NLD) tmem_wait_ld2(va, vb);
-                else if (k + 2 < NLD) tmem_wait_ld(va);
+                for (int p = 0; p < 8; ++p)
+                    acc[k + 1][p] = fma2(pack2(fv(vb[2 * p]), fv(vb[2 * p + 1])), wp, acc[k + 1][p]);
+                if (k + 3 < NC) tmem_ld16(ta + 16 * (k + 3), vb);
+                if (k + 3 < NC) tmem_wait_ld16x2(va, vb);
             }
             tc_fence_before();
             __syncwarp();
@@ -332,7 +355,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
         for (int k = 0; k < NLD; ++k) {
             float vals[32];
 #pragma unroll
-            for (int p = 0; p < 16; ++p) unpack2(acc[k][p], vals[2 * p], vals[2 * p + 1]);
+            for (int p = 0; p < 16; ++p) unpack2(acc[2 * k + (p >> 3)][p & 7], vals[2 * p], vals[2 * p + 1]);
 #pragma unroll
             for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
                 const bool upper = (lane & o) != 0;
@@ -345,29 +368,20 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
             }
             red[q4 * kSlice + h * HALF + 32 * k + lane] = vals[0];
         }
-        // The window's validity, from the same table the producer read (a window
-        // with a bad block id or length was not loaded; its scores are zeros).
-        int ws_, wl_, wh_;
-        window_coords(g, u, ws_, wl_, wh_);
-        const int32_t L = g.len[ws_];
-        const bool len_ok = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
-        if (len_ok) {
-            const int lb = (L - g.W) / g.bs + aidx;  // at most W/16 + 1 <= 65 blocks per window
-            if (lb < (L + g.bs - 1) / g.bs) {
-                const int32_t bid = g.bt[(int64_t)ws_ * g.bt_stride + lb];
-                if (bid < 0 || bid >= g.num_blocks) sh->wbad[j & 1] = j + 1;
-            }
-        }
+        // The window's validity, as the key producer found it in the same table it
+        // loaded from (a window with a bad block id or length was not loaded; its
+        // scores are zeros).
+        const bool wok = wait_phase(smem_u32(&sh->wfull[j & (kWinRing - 1)]), (uint32_t)(j / kWinRing) & 1u, sh, err);
         named_barrier(1, kAcc);
-        const int stat = !len_ok ? KARA_EINVAL : *(volatile int *)&sh->wbad[j & 1] == j + 1 ? KARA_EBADBLOCK : 0;
+        const int stat = wok ? *(volatile int *)&sh->wstat[j & (kWinRing - 1)] : 0;
         if (aidx < S) {
             const float sum = ((red[aidx] + red[kSlice + aidx]) + red[2 * kSlice + aidx]) + red[3 * kSlice + aidx];
             const int key = slice0 + aidx;
             if (key < g.C) scores[u * g.C + key] = stat ? 0.f : sum;
         }
         if (stat && aidx == 0) set_err(err, stat);
-        // the exponential warps marked this window (in this CTA) if a sum left the
-        // safe range; the exact kernel recomputes marked windows
+        // a row total of this window left the safe range (every CTA of the cluster
+        // sees the same totals); the exact kernel recomputes marked windows
         if (aidx == 0 && !stat && *(volatile int *)&sh->unsafe[j & 1] == j + 1) marks[u] = 1;
     }
 }
@@ -384,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sK = base;                                   // two key buffers
     uint8_t *sQ = sK + 2 * C_::kKBytes;                   // two query stages
-    float2 *xs = reinterpret_cast<float2 *>(sQ + 2 * C_::kQBytes);
-    float *red = reinterpret_cast<float *>(xs + kSlots * kSlotFloats2);
+    float *xs = reinterpret_cast<float *>(sQ + 2 * C_::kQBytes);
+    float *red = xs + kSlots * kSlotFloats;
     Shared *sh = reinterpret_cast<Shared *>(red + 4 * kSlice);
     const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
 
@@ -400,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         sh->abort = 0;
         sh->wait_ns = wait_ns;
-        sh->wbad[0] = sh->wbad[1] = 0;
         sh->unsafe[0] = sh->unsafe[1] = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sh->qfull[i]), 1);
@@ -412,9 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&sh->tempty[i]), kAcc / 32);
         }
         for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&sh->xfull[i]), 1);
+        for (int i = 0; i < kWinRing; ++i) mbar_init(smem_u32(&sh->wfull[i]), 1);
         mbar_init(smem_u32(&sh->done), 1);
         fence_mbarrier_init();
-        for (int i = 0; i < kSlots; ++i) mbar_arrive_expect_tx(smem_u32(&sh->xfull[i]), (uint32_t)(ncta * kStrip * 8));
+        for (int i = 0; i < kSlots; ++i) mbar_arrive_expect_tx(smem_u32(&sh->xfull[i]), (uint32_t)(ncta * kStrip * 4));
     }
     if (warp == 13) {
         tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
@@ -459,38 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         reg_dealloc<kRegsCtl>();
         if (warp == 12) {
-            // ---------------- producer: key slices and query strips by TMA --------
-            int issued = 0, kissued = 0;  // query strips, key slices issued
-            // Window j's key slice goes into buffer j & 1, one TMA box per (paged
-            // block, 64-column atom), a block's 16 rows at 16-row steps; a block
-            // id outside the pool reads zeros (the tensor map's bounds) and the
-            // accumulating warps report the window.
-            auto load_k = [&](int j) {
-                const int64_t u = cid + (int64_t)j * nclus;
-                int s, l, h;
-                window_coords(g, u, s, l, h);
-                const int32_t L = g.len[s];
-                const bool ok = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
-                const int x0 = L - g.W + slice0;
-                const int b0 = ok ? x0 / kBlockRows : 0;
-                const int nblk = ok ? (x0 + S - 1) / kBlockRows - b0 + 1 : 0;
-                const int32_t myblk = lane < nblk ? g.bt[(int64_t)s * g.bt_stride + b0 + lane] : 0;
-                const int kb = j & 1;
-                if (lane == 0 && j >= 2) wait_phase(smem_u32(&sh->kempty[kb]), ((j - 2) >> 1) & 1, sh, err);
-                __syncwarp();
-                const uint32_t bar = smem_u32(&sh->kfull[kb]);
-                if (lane == 0 && !stall) mbar_arrive_expect_tx(bar, (uint32_t)(nblk * C_::kAtoms * C_::kBoxBytes));
-                for (int i = 0; i < nblk; ++i) {
-                    const int32_t blk = __shfl_sync(0xffffffffu, myblk, i);
-                    if (lane == 0 && !stall)
-#pragma unroll
-                        for (int a = 0; a < C_::kAtoms; ++a)
-                            tma_load_5d(sK_u + kb * C_::kKBytes + a * kKAtomBytes + i * C_::kBoxBytes, &kmap, bar,
-                                        a * 64, 0, h, blk, l);
-                }
-                kissued = j + 1;
-            };
-            if (nw > 0) load_k(0);
+            // ---------------- query strips by TMA ----------------------------------
+            int issued = 0;
             for (int j = 0; j < nw; ++j) {
                 const int64_t u = cid + (int64_t)j * nclus;
                 int s, l, h;
@@ -515,18 +499,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    // the next window's key slice, once this window's second strip is on its
-                    // way: by then the previous window's MMAs, which read that buffer, are done
-                    if (t == (T > 1 ? 1 : 0) && j + 1 < nw) load_k(j + 1);
                 }
             }
             // drain: every issued copy has landed before this CTA may exit
-            if (lane == 0 && !stall) {
+            if (lane == 0 && !stall)
                 for (int gt = max(0, issued - 2); gt < issued; ++gt)
                     wait_phase(smem_u32(&sh->qfull[gt & 1]), (gt >> 1) & 1, sh, err, false);
+            __syncwarp();
+        } else if (warp == 14) {
+            // ---------------- key slices by TMA ------------------------------------
+            // Window j's key slice goes into buffer j & 1, one TMA box per (paged
+            // block, 64-column atom), a block's 16 rows at 16-row steps; a block
+            // id outside the pool reads zeros (the tensor map's bounds).  The
+            // window's length and all its block ids are read here once: the first
+            // key's row offset goes to the MMA issuer with the buffer, the window's
+            // status to the accumulating warps.
+            int kissued = 0;
+            for (int j = 0; j < nw; ++j) {
+                const int64_t u = cid + (int64_t)j * nclus;
+                int s, l, h;
+                window_coords(g, u, s, l, h);
+                const int32_t L = g.len[s];
+                const bool ok = L >= g.W && ((int64_t)L + g.bs - 1) / g.bs <= g.bt_stride;
+                const int32_t *btr = g.bt + (int64_t)s * g.bt_stride;
+                // every block of the window (at most W/16 + 1 <= 65), as each CTA of
+                // the cluster must reach the same verdict
+                bool bad = false;
+                if (ok)
+                    for (int lb = (L - g.W) / g.bs + lane; lb < (L + g.bs - 1) / g.bs; lb += 32) {
+                        const int32_t bid = btr[lb];
+                        bad |= bid < 0 || bid >= g.num_blocks;
+                    }
+                bad = __any_sync(0xffffffffu, bad);
+                const int x0 = L - g.W + slice0;
+                const int b0 = ok ? x0 / kBlockRows : 0;
+                const int nblk = ok ? (x0 + S - 1) / kBlockRows - b0 + 1 : 0;
+                const int32_t myblk = lane < nblk ? btr[b0 + lane] : 0;
+                const int kb = j & 1;
+                int go = 0;
+                if (lane == 0) {
+                    if (j >= 2) wait_phase(smem_u32(&sh->kempty[kb]), ((j - 2) >> 1) & 1, sh, err);
+                    sh->koff[kb] = ok ? x0 % kBlockRows : 0;
+                    sh->wstat[j & (kWinRing - 1)] = !ok ? KARA_EINVAL : bad ? KARA_EBADBLOCK : 0;
+                    mbar_arrive(smem_u32(&sh->wfull[j & (kWinRing - 1)]));
+                    // after a time-out nothing more is loaded: the buffer may still be
+                    // read, and its barrier still waits for the previous load
+                    go = !stall && !*(volatile int *)&sh->abort;
+                }
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (go) {
+                    const uint32_t bar = smem_u32(&sh->kfull[kb]);
+                    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nblk * C_::kAtoms * C_::kBoxBytes));
+                    for (int i = 0; i < nblk; ++i) {
+                        const int32_t blk = __shfl_sync(0xffffffffu, myblk, i);
+                        if (lane == 0)
+#pragma unroll
+                            for (int a = 0; a < C_::kAtoms; ++a)
+                                tma_load_5d(sK_u + kb * C_::kKBytes + a * kKAtomBytes + i * C_::kBoxBytes, &kmap,
+                                            bar, a * 64, 0, h, blk, l);
+                    }
+                    kissued = j + 1;
+                }
+            }
+            if (lane == 0 && !stall)
                 for (int j = max(0, kissued - 2); j < kissued; ++j)
                     wait_phase(smem_u32(&sh->kfull[j & 1]), (j >> 1) & 1, sh, err, false);
-            }
             __syncwarp();
         } else if (warp == 13) {
             // ---------------- MMA issuer -----------------------------------------
@@ -535,12 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int j = 0; j < nw && ok; ++j) {
                     const int kb = j & 1;
-                    // the window's first key sits o rows into the key buffer
-                    int s, l, h;
-                    window_coords(g, cid + (int64_t)j * nclus, s, l, h);
-                    const int32_t L = g.len[s];
-                    const int o = L >= g.W ? (L - g.W + slice0) % kBlockRows : 0;
                     ok = wait_phase(smem_u32(&sh->kfull[kb]), (j >> 1) & 1, sh, err);
+                    // the window's first key sits o rows into the key buffer
+                    const int o = *(volatile int *)&sh->koff[kb];
                     for (int t = 0; t < T && ok; ++t) {
                         const int gt = j * T + t, st = gt & 1;
                         ok = wait_phase(smem_u32(&sh->qfull[st]), (gt >> 1) & 1, sh, err) &&
@@ -574,6 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // no CTA leaves while a peer may still send to its shared memory
     cluster_arrive();
     cluster_wait();
+    // After a time-out nothing waited for a peer's last partials, which may
+    // still be in flight to this CTA's shared memory: give them time to land.
+    if (*(volatile int *)&sh->abort) {
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < kDrainNs) {
+            }
+        }
+        __syncthreads();
+    }
     if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -215,6 +215,13 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]) : : "memory");
 }
 
+// The same wait for two 16-column loads in flight, both register sets tied.
+__device__ __forceinline__ void tmem_wait_ld16x2(uint32_t (&v)[16], uint32_t (&w)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),
+                 "+r"(w[0]),"+r"(w[1]),"+r"(w[2]),"+r"(w[3]),"+r"(w[4]),"+r"(w[5]),"+r"(w[6]),"+r"(w[7]),"+r"(w[8]),"+r"(w[9]),"+r"(w[10]),"+r"(w[11]),"+r"(w[12]),"+r"(w[13]),"+r"(w[14]),"+r"(w[15]) : : "memory");
+}
+
 // The same wait for two 32-column loads in flight, both register sets tied.
 __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&v)[32], uint32_t (&w)[32])
 {
@@ -320,6 +327,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 // Asynchronous 8-byte store into the shared memory of a CTA of the cluster
 // (`addr` from mapa); completes 8 bytes of transaction count on the mbarrier
 // `bar` (also mapped into that CTA).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(a)), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_async_f2(uint32_t addr, float a, float b, uint32_t bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
