@@ -424,7 +424,8 @@ def main():
         "gpu_launches": None,
         "clocks": clocks,
     }
-    line["gpu_launches"] = args.steps * (launches_per_step() + (1 if args.q_ring else 0))
+    line["gpu_launches"] = args.steps * (launches_per_step(spec.W, args.score_mode == "causal")
+                                         + (1 if args.q_ring else 0))
     if args.q_ring:
         qbytes = nwin * spec.G * (spec.R + spec.B) * spec.d * 2 * 2
         line["phases_ms"]["compact_queries"] = qring_ms
@@ -621,9 +622,12 @@ def run_serve_sim(args, dev):
         print(json.dumps(line), flush=True)
 
 
-def launches_per_step():
-    """Kernels of this library per kara_compress_batch: plan, score, select, compact, commit."""
-    return 5
+def launches_per_step(W, causal):
+    """Kernels of this library per kara_compress_batch: plan, score, select, the
+    fresh-id and kept-row checks, compact, commit.  Bidirectional scoring with
+    W <= 1024 is the single-pass kernel plus the exact recompute of marked
+    windows (two launches); otherwise the two-pass kernel (one)."""
+    return 6 + (2 if (W <= 1024 and not causal) else 1)
 
 
 def profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err):

@@ -85,6 +85,85 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Geo g, int64_t n_fre
     if (threadIdx.x == 0 && carry_new > n_fresh) set_err(err, KARA_ENOBLOCKS);
 }
 
+// The inputs the copy must not run with, checked before it writes anything:
+// the rewrite fills fresh blocks while the batch's old blocks are still read,
+// so a consumed fresh id must be new.
+//   - fresh_check_kernel: every fresh id the plan consumes, fresh[i] for
+//     i < total_new, against the earlier consumed ids and against every entry
+//     below ceil(L/bs) of every table of the batch (a block the batch keeps or
+//     still reads), as raw values: a match records KARA_EDUPBLOCK.  An id
+//     outside [0, num_blocks) records KARA_EBADBLOCK, which a match overrides.
+//   - kept_check_kernel: each window's kept row must be strictly increasing in
+//     [0, C) (Top-K and Token2Chunk produce ascending positions): KARA_EINVAL.
+// Each probe value (a consumed fresh id or a table entry) is compared with the
+// consumed fresh ids through tiles staged in shared memory: no scratch memory,
+// and the work is (total_new + n * bt_stride) * total_new comparisons.
+constexpr int kChkThreads = 256;
+constexpr int kChkProbes = 4;     // probe values per thread
+constexpr int kChkTile = 2048;    // fresh ids per shared-memory tile
+
+__device__ __forceinline__ void record_dup(int32_t *err)
+{
+    if (atomicCAS(err, 0, KARA_EDUPBLOCK) == KARA_EBADBLOCK) atomicCAS(err, KARA_EBADBLOCK, KARA_EDUPBLOCK);
+}
+
+__global__ void __launch_bounds__(kChkThreads) fresh_check_kernel(Geo g, const SeqPlan *__restrict__ plan,
+                                                                  const int32_t *__restrict__ fresh,
+                                                                  int64_t n_fresh, int32_t *err)
+{
+    __shared__ int32_t tile[kChkTile];
+    const SeqPlan last = plan[g.n - 1];
+    const int64_t F = (int64_t)last.off_new + last.n_new;  // fresh ids the plan consumes
+    if (F > n_fresh) return;                                // KARA_ENOBLOCKS is recorded
+    const int64_t P = F + (int64_t)g.n * g.bt_stride;       // probes: consumed ids, then table slots
+    int32_t v[kChkProbes];
+    int64_t lim[kChkProbes];                                // compare with fresh[j], j < lim
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kChkProbes; ++k) {
+        const int64_t p = ((int64_t)blockIdx.x * kChkProbes + k) * kChkThreads + threadIdx.x;
+        v[k] = 0;
+        lim[k] = 0;
+        if (p < F) {
+            v[k] = fresh[p];
+            lim[k] = p;
+            bad |= v[k] < 0 || v[k] >= g.num_blocks;
+        } else if (p < P) {
+            const int64_t q = p - F;
+            const int s = (int)(q / g.bt_stride), lb = (int)(q % g.bt_stride);
+            const int64_t L = g.len[s];
+            if (L > 0 && lb < (L + g.bs - 1) / g.bs) {
+                v[k] = g.bt[q];
+                lim[k] = F;
+            }
+        }
+    }
+    bool dup = false;
+    for (int64_t t0 = 0; t0 < F; t0 += kChkTile) {
+        const int n = (int)min((int64_t)kChkTile, F - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += kChkThreads) tile[i] = fresh[t0 + i];
+        __syncthreads();
+        for (int i = 0; i < n; ++i) {
+            const int32_t f = tile[i];
+#pragma unroll
+            for (int k = 0; k < kChkProbes; ++k) dup |= f == v[k] && t0 + i < lim[k];
+        }
+    }
+    if (bad) atomicCAS(err, 0, KARA_EBADBLOCK);
+    if (dup) record_dup(err);
+}
+
+__global__ void __launch_bounds__(kChkThreads) kept_check_kernel(int64_t n, int R, int C,
+                                                                 const int32_t *__restrict__ kept, int32_t *err)
+{
+    for (int64_t i = (int64_t)blockIdx.x * kChkThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kChkThreads) {
+        const int r = (int)(i % R);
+        const int32_t k = kept[i];
+        if (k < 0 || k >= C || (r > 0 && kept[i - 1] >= k)) set_err(err, KARA_EINVAL);
+    }
+}
+
 // One block per (window, K|V): copies o + R + B rows of D bf16 with 16-byte
 // vector loads/stores, old rows read through the old table, new rows written
 // into the sequence's fresh blocks.
@@ -96,6 +175,8 @@ __global__ void __launch_bounds__(256) compact_kernel(Geo g, const SeqPlan *__re
 {
     constexpr int CPR = D * 2 / 16;  // 16-byte chunks per row
     constexpr int UNROLL = 4;
+    // nothing is written once an earlier kernel (plan, checks) recorded an error
+    if (*(volatile const int32_t *)err != 0) return;
     const int64_t u = blockIdx.x >> 1;
     const int which = blockIdx.x & 1;
     int s, l, h;
@@ -177,11 +258,22 @@ cudaError_t launch_plan(const Geo &g, int64_t n_fresh, SeqPlan *plan, int32_t *e
     return cudaGetLastError();
 }
 
+// The checks, then the copy (which runs only if no error was recorded).
 cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
                            int64_t n_fresh, int32_t *err, cudaStream_t st)
 {
     const int64_t blocks = g.nwin * 2;
     if (blocks == 0) return cudaSuccess;
+    {
+        const int64_t probes = n_fresh + (int64_t)g.n * g.bt_stride;
+        const int64_t per = (int64_t)kChkThreads * kChkProbes;
+        const int64_t nb = (probes + per - 1) / per;
+        if (nb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        fresh_check_kernel<<<(unsigned)nb, kChkThreads, 0, st>>>(g, plan, fresh, n_fresh, err);
+        const int64_t nk = g.nwin * g.R;
+        const int64_t kb = (nk + kChkThreads - 1) / kChkThreads;
+        kept_check_kernel<<<(unsigned)(kb < 4096 ? kb : 4096), kChkThreads, 0, st>>>(nk, g.R, g.C, kept, err);
+    }
     if (g.D == 128)
         compact_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(g, plan, kept, fresh, n_fresh, err);
     else

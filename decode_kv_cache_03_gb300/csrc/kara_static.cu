@@ -8,8 +8,6 @@
 // needs -- the per-sequence page plan -- in a fixed array compiled into the
 // library instead.  It runs the same plan, copy and commit kernels as
 // kara_compact; only where the plan lives differs.
-#include <atomic>
-
 #include "kara_common.cuh"
 
 using namespace kara;
@@ -20,26 +18,16 @@ static __device__ __align__(256) SeqPlan g_static_plan[KARA_STATIC_MAX_SEQS];
 
 namespace {
 
-constexpr int kMaxDevices = 256;
-
-// Device address of g_static_plan, looked up once per device.  In host code
-// the array's name denotes a host-side stand-in, not device memory, so the
-// kernels are always given this looked-up address.
-std::atomic<SeqPlan *> g_plan_addr[kMaxDevices];
-
+// Device address of g_static_plan in the current context.  In host code the
+// array's name denotes a host-side stand-in, not device memory, so the kernels
+// are given this looked-up address.  It is looked up on every call (a host-side
+// query that allocates nothing): a cached address would outlive the context
+// it came from, e.g. across cudaDeviceReset.
 kara_status static_plan(SeqPlan **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KARA_ECUDA;
-    if (dev < 0 || dev >= kMaxDevices) return KARA_EUNSUPPORTED;
-    SeqPlan *p = g_plan_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_static_plan) != cudaSuccess || !addr) return KARA_ECUDA;
-        p = static_cast<SeqPlan *>(addr);
-        g_plan_addr[dev].store(p, std::memory_order_release);
-    }
-    *out = p;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_static_plan) != cudaSuccess || !addr) return KARA_ECUDA;
+    *out = static_cast<SeqPlan *>(addr);
     return KARA_OK;
 }
 

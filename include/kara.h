@@ -54,7 +54,7 @@ typedef enum {
     KARA_EINVAL = -1,        /* an argument or a cached length is out of range */
     KARA_EUNSUPPORTED = -2,  /* a shape outside the supported set above */
     KARA_ENOBLOCKS = -3,     /* the fresh-block list is shorter than the plan needs */
-    KARA_EDUPBLOCK = -4,     /* reserved */
+    KARA_EDUPBLOCK = -4,     /* a fresh block id repeats, or is a block the batch still lists (device) */
     KARA_ECUDA = -5,         /* a CUDA runtime call failed (launch or attribute) */
     KARA_EBADBLOCK = -6,     /* a block id outside [0, num_blocks) (device) */
     KARA_ETIMEOUT = -7,      /* a bounded device-side wait ran out (device) */
@@ -253,6 +253,18 @@ kara_status kara_select(const kara_params *p, int64_t n_windows, const float *sc
  * [p0 + n_new, ceil(L/bs)) become -1, the released ids go to `freed` (in
  * sequence order) and new_len[s] = L'.  If *err is non-zero nothing is
  * committed: the table is unchanged, freed is untouched, new_len[s] = L.
+ * Before anything is written the device checks (the pages give no rule: these
+ * follow from filling caller-supplied blocks while the old ones are still
+ * read) and records, with this precedence:
+ *   KARA_EDUPBLOCK  a fresh id the plan consumes (fresh[i], i < total_new)
+ *                   equals an earlier consumed id or an entry below
+ *                   ceil(L/bs) of any table of the batch (values compared as
+ *                   given; ids past total_new are never read);
+ *   KARA_EBADBLOCK  a consumed fresh id outside [0, num_blocks);
+ *   KARA_EINVAL     a kept row that is not strictly increasing in [0, C).
+ * With any of these (or a plan error) no block is written.  An old block id
+ * outside the pool, met while copying, records KARA_EBADBLOCK: fresh blocks
+ * may then have been written, live blocks never are.
  * kept [n][num_layers][num_kv_heads][R]; fresh [n_fresh] (at least the plan's
  * total_new); freed [total_old]; new_len [n].
  * ws/ws_bytes: workspace of kara_workspace_size bytes.
@@ -292,14 +304,15 @@ kara_status kara_get_error(const int32_t *err, kara_stream_t stream);
  * engine whose memory pool handed all free HBM to the KV cache at start-up,
  * or a host program that embeds this library without any device allocator.
  * Such a caller passes its inputs and outputs exactly as for kara_compact
- * (same meaning, layout, ownership and commit rule) but no workspace; the
+ * (same meaning, layout, ownership, checks and commit rule) but no workspace; the
  * per-sequence plan lives in a fixed array inside the library instead:
  * KARA_STATIC_MAX_SEQS entries of 32 bytes (256 KiB), held by every GPU that
  * loads the library until the process exits.
  *   - More than KARA_STATIC_MAX_SEQS sequences: returns KARA_EUNSUPPORTED
  *     before any device work.  Split the batch.
- *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - Each call looks up the array's device address in the current context
+ *     (a host-side query that allocates nothing), so no address is kept past
+ *     the context it belongs to (for example across cudaDeviceReset).
  *   - Every call uses the same array and it keeps the last call's contents.
  *     Nothing has to be cleared between calls (each call writes every entry
  *     it reads), but calls whose work overlaps on the GPU -- two streams with
