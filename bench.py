@@ -22,6 +22,7 @@ import sys
 import tempfile
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -130,10 +131,12 @@ class ClockSampler:
         return out
 
 
-def cpu_oracle_sample(wl_dev, seqs, layers_sample, threads=None):
+def cpu_oracle_sample(wl_dev, seqs, layers_sample, threads=None, keep=False):
     """Time the oracle (as it stands) on a bounded sample: the windows of a few
     sequences and layers of the same workload, on `threads` host threads (all
-    cores by default).  Returns (windows/s, seconds, threads, windows)."""
+    cores by default).  Returns (windows/s, seconds, threads, windows), and with
+    keep=True also what the parity check needs: the oracle's scores, cand and
+    kept, the shape and the host sub-workload."""
     import oracle
     sub = synth.host_subset(wl_dev, seqs)
     spec = sub.spec.with_(layers=layers_sample)
@@ -145,12 +148,91 @@ def cpu_oracle_sample(wl_dev, seqs, layers_sample, threads=None):
     threads = threads or oracle.max_threads()
     t0 = time.perf_counter()
     sc = oracle.scores(sh, q, k, sub.block_table, sub.lengths, nthreads=threads)
-    _, kept = oracle.select_batch(sc, spec.K, spec.R, spec.lam, nthreads=threads)
+    cand, kept = oracle.select_batch(sc, spec.K, spec.R, spec.lam, nthreads=threads)
     st = oracle.compact(sh, k, v, sub.block_table, sub.lengths, kept, sub.fresh)[0]
     dt = time.perf_counter() - t0
     assert st == oracle.OK
     nwin = spec.n_seq * spec.layers * spec.hkv
+    if keep:
+        return nwin / dt, dt, threads, nwin, dict(sc=sc, cand=cand, kept=kept, sh=sh, sub=sub, k=k, v=v)
     return nwin / dt, dt, threads, nwin
+
+
+def window_rows(kpool, vpool, bt, lengths, W, B, R, bs, layers):
+    """K and V rows of the rebuilt region [p0*bs, L') of each sequence's window,
+    read through a table: [seq] -> (k [rows][layers][hkv][D], v alike), raw bits."""
+    out = []
+    for s in range(bt.shape[0]):
+        L = int(lengths[s])
+        p0 = (L - W) // bs
+        x = np.arange(p0 * bs, L - (W - B) + R)
+        blk = np.asarray(bt[s])[x // bs].astype(np.int64)
+        slot = x % bs
+        if isinstance(kpool, torch.Tensor):      # gathered on the device, then copied
+            bi = torch.from_numpy(blk).to(kpool.device)
+            si = torch.from_numpy(slot).to(kpool.device)
+            out.append((kpool[:layers][:, bi, :, si, :].cpu().numpy(),
+                        vpool[:layers][:, bi, :, si, :].cpu().numpy()))
+        else:
+            out.append((kpool[:layers][:, blk, :, slot, :], vpool[:layers][:, blk, :, slot, :]))
+    return out
+
+
+def parity_sample(kara, spec, c, p, b, bt, bt0, fresh, freed, new_len, ws, err, wl, seqs, layers, ref):
+    """The GPU's outputs on the oracle's sample windows, compared with the oracle:
+    scores (max relative error), selection (exact kept/cand rows: on the oracle's
+    own scores, on the windows whose oracle selection is stable under 1e-4
+    relative noise, and on the GPU's scores, where it must be exact), and
+    compaction (the bytes of every rebuilt row, the oracle compacting with the
+    GPU's kept)."""
+    import oracle
+    dev = wl.q.device
+    scores = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.C, dtype=torch.float32, device=dev)
+    cand = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.K, dtype=torch.int32, device=dev)
+    kept = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.R, dtype=torch.int32, device=dev)
+    bt.copy_(bt0)
+    kara.kara_compress_batch(c, p, b, fresh, freed, new_len, ws, err, scores_out=scores, cand_out=cand,
+                             kept_out=kept)
+    assert kara.kara_get_error(err) == 0
+    g_sc = scores[seqs, :layers].cpu().numpy()
+    g_cand = cand[seqs, :layers].cpu().numpy()
+    g_kept = kept[seqs, :layers].cpu().numpy()
+    g_bt = bt[seqs].cpu().numpy()
+    g_rows = window_rows(wl.k.view(torch.int16), wl.v.view(torch.int16), g_bt, wl.lengths[seqs].cpu().numpy(),
+                         spec.W, spec.B, spec.R, spec.block, layers)
+    bt.copy_(bt0)
+    torch.cuda.synchronize()
+    rel = np.abs(g_sc.astype(np.float64) - ref["sc"].astype(np.float64)) / np.maximum(np.abs(ref["sc"]), 1e-30)
+    C = spec.C
+    flat = ref["sc"].reshape(-1, C)
+    base = ref["kept"].reshape(-1, spec.R)
+    rng = np.random.default_rng(0)
+    stable = np.ones(flat.shape[0], bool)
+    for _ in range(6):
+        pert = (flat * (1 + 1e-4 * rng.uniform(-1, 1, flat.shape))).astype(np.float32)
+        stable &= np.all(oracle.select_batch(pert, spec.K, spec.R, spec.lam)[1] == base, axis=-1)
+    kept_eq = np.all(g_kept.reshape(-1, spec.R) == base, axis=-1)
+    cand_eq = np.all(g_cand.reshape(-1, spec.K) == ref["cand"].reshape(-1, spec.K), axis=-1)
+    o_cand, o_kept = oracle.select_batch(g_sc.reshape(-1, C), spec.K, spec.R, spec.lam)
+    same_in = np.all(o_kept == g_kept.reshape(-1, spec.R), axis=-1) & np.all(o_cand == g_cand.reshape(-1, spec.K),
+                                                                              axis=-1)
+    sub = ref["sub"]
+    st, k2, v2, bt2, _, nl2 = oracle.compact(ref["sh"], ref["k"], ref["v"], sub.block_table, sub.lengths, g_kept,
+                                             sub.fresh)
+    assert st == oracle.OK
+    o_rows = window_rows(k2, v2, bt2, sub.lengths.numpy(), spec.W, spec.B, spec.R, spec.block, layers)
+    mism = sum(int(np.count_nonzero(a.view(np.uint16) != b.view(np.uint16)))
+               for (ga, gb), (oa, ob) in zip(g_rows, o_rows) for a, b in ((ga, oa), (gb, ob)))
+    nbytes = sum(a.size * 2 for ga, gb in g_rows for a in (ga, gb))
+    n = flat.shape[0]
+    return {"sample": f"{n} windows ({len(seqs)} sequences x {layers} layers x {spec.hkv} KV heads) of the "
+                      f"timed workload; oracle: fp64 scores, selection, compaction",
+            "max_rel_score_err": float(rel.max()), "score_rtol": 1e-3,
+            "kept_exact": float(kept_eq.mean()), "cand_exact": float(cand_eq.mean()),
+            "stable_windows": int(stable.sum()), "kept_exact_on_stable": float(kept_eq[stable].mean())
+            if stable.any() else None,
+            "selection_exact_given_gpu_scores": float(same_in.mean()),
+            "compaction_bytes_compared": int(nbytes), "compaction_byte_mismatches": mism}
 
 
 def dist_setup():
@@ -436,7 +518,7 @@ def main():
         bt.copy_(bt0)
         torch.cuda.synchronize()
         nl = sample_layers(wl, sample_seqs)
-        rate, dt, thr, sw = cpu_oracle_sample(wl, sample_seqs, nl)
+        rate, dt, thr, sw, ref = cpu_oracle_sample(wl, sample_seqs, nl, keep=True)
         line["cpu_baseline"] = {"value": rate, "unit": "windows/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{sw} windows ({len(sample_seqs)} sequences x {nl} layers x "
                                           f"{spec.hkv} KV heads) of the same workload, {dt:.1f} s"}
@@ -445,6 +527,9 @@ def main():
         line["cpu_baseline"]["single_core"] = {"value": rate1, "unit": "windows/s", "cores": 1,
                                                "sample": f"{sw1} windows (1 sequence x 1 layer x {spec.hkv} KV "
                                                          f"heads), {dt1:.1f} s"}
+        if not args.q_ring and args.score_mode == "bidirectional" and args.select_mode == "token2chunk":
+            line["parity"] = parity_sample(kara, spec, c, p, b, bt, bt0, fresh, freed, new_len, ws, err, wl,
+                                           sample_seqs, nl, ref)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_ > 1:
