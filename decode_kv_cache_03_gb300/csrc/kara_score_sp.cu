@@ -81,9 +81,9 @@ constexpr int kThreads = 512;  // warpgroups: exponentials, accumulation x2, TMA
 // launch bounds), then after the warpgroups trade registers.  The trade must
 // add up: 128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch.
 constexpr int kRegsLaunch = 128;
-constexpr uint32_t kRegsExp = 72;
+constexpr uint32_t kRegsExp = 80;
 constexpr uint32_t kRegsAcc = 192;
-constexpr uint32_t kRegsCtl = 56;
+constexpr uint32_t kRegsCtl = 48;
 static_assert(128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch, "register trade must add up");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
@@ -261,14 +261,15 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                 unpack2(z4[i], lo, hi);
                 z += lo + hi;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            // after a time-out the exchange stops: nothing more is sent
+            // the row's partial goes out first (it does not depend on the TMEM
+            // stores); after a time-out the exchange stops: nothing more is sent
             if (!*(volatile int *)&sh->abort) {
                 const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotFloats + (int)crank * kStrip + row);
                 const uint32_t xb = smem_u32(&sh->xfull[slot]);
                 for (int c = 0; c < ncta; ++c) st_async_f32(mapa(xl, (uint32_t)c), z, mapa(xb, (uint32_t)c));
             }
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sh->eready[b]));
         }
