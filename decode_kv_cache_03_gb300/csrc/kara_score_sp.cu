@@ -297,6 +297,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
     for (int j = 0; j < nw; ++j) {
         const int64_t u = cid + (int64_t)j * nclus;
         uint64_t acc[NC][8];
+        bool bad = false;  // a row total of this window left the safe range
 #pragma unroll
         for (int k = 0; k < NC; ++k)
 #pragma unroll
@@ -322,8 +323,10 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
             // rows past G*W (the tail of the last strip) add nothing; a row total
             // out of the safe range marks the window for the exact recompute
             const bool live = got && t * kStrip + row < GW;
-            if (live && !in_safe_range(Z)) *(volatile int *)&sh->unsafe[j & 1] = j + 1;
-            const float w = (live && in_safe_range(Z)) ? rcp_approx(Z) : 0.f;
+            bad |= live && !in_safe_range(Z);
+            // (the reciprocal on the FMA pipe: the special-function unit is busy
+            // with the exponential warps' stream)
+            const float w = (live && in_safe_range(Z)) ? rcp_newton(Z) : 0.f;
             const uint64_t wp = pack2(w, w);
             tmem_wait_ld16x2(va, vb);
 #pragma unroll
@@ -351,6 +354,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
         // round with offset o a lane keeps the half of its range selected by bit o
         // of its lane id) leaves lane l with key 32k + l summed over the warp's 32
         // rows; the four lane quarters are added through shared memory below.
+        if (bad) *(volatile int *)&sh->unsafe[j & 1] = j + 1;
         named_barrier(1, kAcc);  // the previous window's sums have been read
 #pragma unroll
         for (int k = 0; k < NLD; ++k) {

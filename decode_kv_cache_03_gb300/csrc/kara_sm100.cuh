@@ -441,6 +441,19 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t y2)
     return pack2(r0, r1);
 }
 
+// 1/x on the FMA pipe, for x in [2^-120, 2^120]: the exponent-flip guess
+// 2^127 / x read off the bit pattern (0x7F000000 - bits(x), relative error at
+// most 1/8) and three Newton steps y <- y (2 - x y), each squaring the error
+// (1/8 -> 2^-6 -> 2^-12 -> 2^-24, plus rounding).
+__device__ __forceinline__ float rcp_newton(float x)
+{
+    float y = __uint_as_float(0x7F000000u - __float_as_uint(x));
+    y = y * fmaf(-x, y, 2.f);
+    y = y * fmaf(-x, y, 2.f);
+    y = y * fmaf(-x, y, 2.f);
+    return y;
+}
+
 // Scalar form of exp2_poly2 (same coefficients and steps).
 __device__ __forceinline__ float exp2_poly(float y)
 {
