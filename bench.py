@@ -47,7 +47,7 @@ def measured_traffic(nwin):
     windows; None when the scorer's sources changed since the capture."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "score_tc_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "score_sp_traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.sha256()
         for src in rec["sources"]:
@@ -479,7 +479,8 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": tf_sus, "unit": "TFLOP/s",
                 "frac": achieved_tflops / tf_sus, "peak_kind": f"{src} sustained bf16",
                 "frac_vs_burst": achieved_tflops / tf_burst}
-    roof.update({"traffic": measured_traffic(nwin) if args.config == "qwen3_14b" else None,
+    roof.update({"traffic": measured_traffic(nwin) if (args.config == "qwen3_14b" and args.score_mode == "bidirectional")
+                 else None,
                  "traffic_unit": "bytes per launch (DRAM read + write)", "algorithmic_bytes": score_bytes,
                  "kernel": "window scoring (QK^T, softmax, column sums)"})
     line = {
