@@ -145,6 +145,42 @@ def test_score_shapes(G, W, B, D):
     assert e.max() <= SCORE_RTOL, f"max rel err {e.max():.3e} at {np.unravel_index(e.argmax(), e.shape)}"
 
 
+@pytest.mark.parametrize("scale,W", [(60.0, 384), (-1e-3, 512)])
+def test_windows_outside_the_single_pass_range_are_recomputed(scale, W):
+    """The single-pass scorer exponentiates against the log-sum-exp of the same
+    row position two strips earlier.  Here the query rows of the window's third
+    strip are scaled so that reference is far off: by 60 (logits ~2^250 above
+    it, the fp32 exponentials overflow) or by a tiny negative factor with the
+    earlier strips' logits large (every term underflows).  Those windows must
+    leave the single-pass arithmetic's range, be marked, and be recomputed
+    exactly, so the scores still match the oracle."""
+    kara = lib()
+    spec = random_spec(931, G=1, hkv=2, W=W, B=32, D=128, n_seq=2, layers=1, len_lo=W, len_hi=W + 40)
+    wl = synth.generate(spec)
+    q = wl.q.float()
+    if scale > 0:
+        q[..., 256:, :] *= scale                   # strip 2 (rows 256..) of every window
+    else:
+        q[..., :256, :] *= 60.0                    # strips 0 and 1 large, strip 2 tiny
+        q[..., 256:, :] *= -scale
+    wl = synth.Workload(spec, q.to(torch.bfloat16), wl.k, wl.v, wl.lengths, wl.block_table, wl.fresh,
+                        wl.prefix_pool, wl.fresh_base)
+    d = to_device(wl)
+    c = kara.cache(d.k, d.v, spec.hq)
+    p = kara.params(spec.W, spec.B, 1, 1, spec.lam)
+    b = kara.batch(d.lengths, d.block_table, d.q)
+    scores = torch.full((spec.n_seq, spec.layers, spec.hkv, spec.C), -1.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kara.kara_score(c, p, b, scores, ws, err)
+    assert kara.kara_get_error(err) == 0
+    ref = oracle.scores(oracle.shape_of(wl), wl.q, wl.k, wl.block_table, wl.lengths)
+    got = scores.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    e = rel_err(got, ref)
+    assert e.max() <= SCORE_RTOL, f"max rel err {e.max():.3e} at {np.unravel_index(e.argmax(), e.shape)}"
+
+
 def test_compact_alone_with_oracle_kept():
     kara = lib()
     spec = random_spec(6, G=2, hkv=2, W=128, B=16, D=64, n_seq=3, layers=2, R=30, len_lo=128, len_hi=300)
