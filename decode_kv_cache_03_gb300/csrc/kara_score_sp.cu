@@ -21,13 +21,13 @@
 //     through a TMA ring in 128-row strips.
 //   * Per strip, S = Q_strip * K_slice^T (M = 128 rows, N = slice) goes into
 //     one of two TMEM buffers.
-//   * Exponential warps (one per TMEM lane quarter; a thread owns one query row
-//     and all of the slice's keys) turn the strip's logits into
+//   * Exponential warps (two per TMEM lane quarter; a thread owns one query row
+//     and half of the slice's keys) turn the strip's logits into
 //     e = 2^(l2 - r), l2 = <q,k> log2(e)/sqrt(D), written back over S in TMEM,
-//     and send the CTA's partial sum z = sum e of the row to every CTA of the
+//     and send their partial sum z = sum e of the row to every CTA of the
 //     cluster with st.async (DSMEM, completing bytes on the receiver's
 //     mbarrier).  The reference r is common to the cluster: the row position's
-//     log-sum-exp two strips earlier, r + log2(sum_c z_c), which every CTA
+//     log-sum-exp two strips earlier, r + log2(sum z), which every CTA
 //     derives from the same exchanged partials in the same order (two strips
 //     back, that exchange has long completed).  So no pass over the logits
 //     precedes the exponentials, and the row's normaliser is a plain sum.  A strip whose row total sum_c z_c leaves [2^-88, 2^119] --
@@ -48,12 +48,13 @@
 // The kernel is persistent: each cluster walks its share of the windows, and
 // the next window's key slice loads into the second key buffer while the
 // current window is scored.  No W x W matrix and no per-row statistic reaches
-// global memory; every score is a deterministic fp32 sum.  Warp roles (512
-// threads): warps 0..3 exponentials, 4..11 accumulation, 12 query-strip TMA,
-// 13 TMEM allocation and MMAs (one lane), 14 key-slice TMA (it also reads the
-// window's length and block ids once and publishes the first key's row offset
-// and the window's validity in shared memory), 15 idle; the warpgroups trade
-// registers so the accumulating warps hold 128 accumulators each.  Every wait is bounded;
+// global memory; every score is a deterministic fp32 sum.  Warp roles (640
+// threads): warps 0..7 exponentials (two per lane quarter, one per half of the
+// keys), 8..15 accumulation, 16 query-strip TMA, 17 TMEM allocation and MMAs
+// (one lane), 18 key-slice TMA (it also reads the window's length and block ids
+// once and publishes the first key's row offset and the window's validity in
+// shared memory), 19 idle; the warpgroups trade registers so the accumulating
+// warps hold 128 accumulators each.  Every wait is bounded;
 // on time-out the CTA records KARA_ETIMEOUT and stops waiting, still draining
 // what it has in flight.
 #include <cuda.h>
@@ -75,16 +76,21 @@ constexpr int kSlice = 256;    // keys per CTA
 constexpr int kStrip = 128;    // query rows per strip
 constexpr int kMaxCta = 4;     // CTAs per cluster: W <= 1024
 constexpr int kSlots = 4;      // exchange slots (strips in flight between CTAs)
+constexpr int kExpW = 8;       // exponential warps: two per TMEM lane quarter (column halves)
 constexpr int kAcc = 256;      // accumulating threads: two per TMEM lane
-constexpr int kThreads = 512;  // warpgroups: exponentials, accumulation x2, TMA/MMA
-// Registers per thread: at launch (65536 / 512, what ptxas assigns under the
-// launch bounds), then after the warpgroups trade registers.  The trade must
-// add up: 128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch.
-constexpr int kRegsLaunch = 128;
-constexpr uint32_t kRegsExp = 80;
-constexpr uint32_t kRegsAcc = 192;
+constexpr int kAccW0 = kExpW;  // first accumulating warp
+constexpr int kCtlW0 = kExpW + kAcc / 32;    // control warps: query TMA, MMA, key TMA, idle
+constexpr int kThreads = 32 * (kCtlW0 + 4);  // five warpgroups
+// Registers per thread: at launch (65536 / 640 rounded down to the allocation
+// granule of 8, what ptxas assigns under the launch bounds), then after the
+// warpgroups trade registers.  The trade must add up:
+// 256 * kRegsExp + 256 * kRegsAcc + 128 * kRegsCtl == 640 * kRegsLaunch.
+constexpr int kRegsLaunch = 96;
+constexpr uint32_t kRegsExp = 40;
+constexpr uint32_t kRegsAcc = 176;
 constexpr uint32_t kRegsCtl = 48;
-static_assert(128 * (kRegsExp + kRegsCtl) + 256 * kRegsAcc == 512 * kRegsLaunch, "register trade must add up");
+static_assert(256 * kRegsExp + 256 * kRegsAcc + 128 * kRegsCtl == kThreads * kRegsLaunch,
+              "register trade must add up");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr uint64_t kDrainNs = 20000ull;  // landing time allowed to DSMEM stores after a time-out
@@ -127,8 +133,8 @@ struct Shared {
     int wstat[kWinRing];             // a window's status: 0, KARA_EINVAL or KARA_EBADBLOCK
 };
 
-// Exchange slot: the partial sum of every CTA for each row.
-constexpr int kSlotFloats = kMaxCta * kStrip;
+// Exchange slot: the partial sums of every CTA for each row, one per column half.
+constexpr int kSlotFloats = kMaxCta * 2 * kStrip;
 
 template <int D>
 size_t smem_bytes()
@@ -171,46 +177,48 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Shared
 
 __device__ __forceinline__ float fv(uint32_t x) { return __uint_as_float(x); }
 
-// Row total of an exchange slot: the CTAs' partial sums added in CTA order, so
-// every CTA of the cluster (and both warp roles) gets the same value.
+// Row total of an exchange slot: the partial sums added in (CTA, half) order,
+// so every CTA of the cluster (and both warp roles) gets the same value.
 __device__ __forceinline__ float slot_total(const float *xs, int slot, int ncta, int row)
 {
-    float Z = xs[slot * kSlotFloats + row];
+    float Z = xs[slot * kSlotFloats + row] + xs[slot * kSlotFloats + kStrip + row];
 #pragma unroll
     for (int c = 1; c < kMaxCta; ++c)
-        if (c < ncta) Z += xs[slot * kSlotFloats + c * kStrip + row];
+        if (c < ncta)
+            Z += xs[slot * kSlotFloats + (2 * c) * kStrip + row] + xs[slot * kSlotFloats + (2 * c + 1) * kStrip + row];
     return Z;
 }
 
 __device__ __forceinline__ bool in_safe_range(float Z) { return Z >= kSumLo && Z <= kSumHi; }  // NaN: false
 
-// v[i] <- 2^(v[i]*c2 - r) in place (raw bits) for the 16 values, z += them as
-// 4 packed pairs of partial sums.
-__device__ __forceinline__ void exp16(uint32_t (&v)[16], uint64_t c2p, uint64_t nrp, uint64_t (&z)[4])
+// v[i] <- 2^(v[i]*c2 - r) in place (raw bits) for the 8 values, z += them as
+// 2 packed pairs of partial sums.
+__device__ __forceinline__ void exp8(uint32_t (&v)[8], uint64_t c2p, uint64_t nrp, uint64_t (&z)[2])
 {
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
+    for (int i = 0; i < 8; i += 2) {
         const uint64_t y = fma2(pack2(fv(v[i]), fv(v[i + 1])), c2p, nrp);
         float y0, y1;
         unpack2(y, y0, y1);
         const float e0 = ex2(y0), e1 = ex2(y1);
         v[i] = __float_as_uint(e0);
         v[i + 1] = __float_as_uint(e1);
-        z[(i >> 1) & 3] = add2(z[(i >> 1) & 3], pack2(e0, e1));
+        z[(i >> 1) & 1] = add2(z[(i >> 1) & 1], pack2(e0, e1));
     }
 }
 
-// Exponential warps: one per TMEM lane quarter, a thread per query row of the
-// strip and all S = 64 * NLD keys of the slice.
+// Exponential warps: two per TMEM lane quarter, a thread per query row of the
+// strip and half (32 * NLD) of the slice's keys.
 template <int NLD>
 __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float *xs,
                                          int ncta, int T, float c2, int nw)
 {
-    constexpr int NCH = 4 * NLD;  // 16-column chunks
+    constexpr int NCH = 4 * NLD;  // 8-column chunks of this warp's half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = 32 * warp + lane;
+    const int q4 = warp & 3, eh = warp >> 2;
+    const int row = 32 * q4 + lane;
     const uint32_t crank = cluster_ctarank();
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const uint64_t c2p = pack2(c2, c2);
     const uint32_t xs_u = smem_u32(xs);
     // references of this row position for even and odd strips, the same in every
@@ -232,39 +240,40 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                 }
             }
             const float r = rr[b];
-            const uint32_t ta = tmem + lane_base + b * 256;
+            const uint32_t ta = tmem + lane_base + b * 256 + eh * (32 * NLD);
             wait_phase(smem_u32(&sh->tfull[b]), (gt >> 1) & 1, sh, err);
             __syncwarp();  // the TMEM accesses below are warp-collective
             tc_fence_after();
-            uint64_t z4[4] = {0, 0, 0, 0};
+            uint64_t z2[2] = {0, 0};
             const uint64_t nrp = pack2(-r, -r);
             {
-                // two 16-column register sets: chunk c+1 loads while chunk c is
-                // exponentiated (one tcgen05.wait::ld covers all loads in flight)
-                uint32_t ua[16], ub[16];
-                tmem_ld16(ta, ua);
-                tmem_wait_ld16(ua);
+                // two 8-column register sets: chunk c+1 loads while chunk c is
+                // exponentiated (one tcgen05.wait::ld covers all loads in flight);
+                // the two warps of a lane quarter interleave on the SMSP
+                uint32_t ua[8], ub[8];
+                tmem_ld8(ta, ua);
+                tmem_wait_ld8(ua);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    uint32_t(&cur)[16] = (c & 1) ? ub : ua;
-                    uint32_t(&nxt)[16] = (c & 1) ? ua : ub;
-                    if (c + 1 < NCH) tmem_ld16(ta + 16 * (c + 1), nxt);
-                    exp16(cur, c2p, nrp, z4);
-                    tmem_st16(ta + 16 * c, cur);
-                    if (c + 1 < NCH) tmem_wait_ld16(nxt);
+                    uint32_t(&cur)[8] = (c & 1) ? ub : ua;
+                    uint32_t(&nxt)[8] = (c & 1) ? ua : ub;
+                    if (c + 1 < NCH) tmem_ld8(ta + 8 * (c + 1), nxt);
+                    exp8(cur, c2p, nrp, z2);
+                    tmem_st8(ta + 8 * c, cur);
+                    if (c + 1 < NCH) tmem_wait_ld8(nxt);
                 }
             }
             float z = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 float lo, hi;
-                unpack2(z4[i], lo, hi);
+                unpack2(z2[i], lo, hi);
                 z += lo + hi;
             }
             // the row's partial goes out first (it does not depend on the TMEM
             // stores); after a time-out the exchange stops: nothing more is sent
             if (!*(volatile int *)&sh->abort) {
-                const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotFloats + (int)crank * kStrip + row);
+                const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotFloats + (2 * (int)crank + eh) * kStrip + row);
                 const uint32_t xb = smem_u32(&sh->xfull[slot]);
                 for (int c = 0; c < ncta; ++c) st_async_f32(mapa(xl, (uint32_t)c), z, mapa(xb, (uint32_t)c));
             }
@@ -287,12 +296,12 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
     constexpr int HALF = 32 * NLD;
     constexpr int NC = 2 * NLD;  // 16-column chunks of this thread's half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int aw = warp - 4, q4 = warp & 3, h = aw >> 2;  // TMEM lane quarter, column half
+    const int aw = warp - kAccW0, q4 = warp & 3, h = aw >> 2;  // TMEM lane quarter, column half
     const int row = 32 * q4 + lane;
     const int aidx = aw * 32 + lane;
     const int GW = g.G * g.W;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    const uint32_t xbytes = (uint32_t)(ncta * kStrip * 4);  // one slot's bytes from all CTAs
+    const uint32_t xbytes = (uint32_t)(ncta * 2 * kStrip * 4);
 
     for (int j = 0; j < nw; ++j) {
         const int64_t u = cid + (int64_t)j * nclus;
@@ -426,20 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&sh->kfull[i]), 1);
             mbar_init(smem_u32(&sh->kempty[i]), 1);
             mbar_init(smem_u32(&sh->tfull[i]), 1);
-            mbar_init(smem_u32(&sh->eready[i]), 4);
+            mbar_init(smem_u32(&sh->eready[i]), kExpW);
             mbar_init(smem_u32(&sh->tempty[i]), kAcc / 32);
         }
         for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&sh->xfull[i]), 1);
         for (int i = 0; i < kWinRing; ++i) mbar_init(smem_u32(&sh->wfull[i]), 1);
         mbar_init(smem_u32(&sh->done), 1);
         fence_mbarrier_init();
-        for (int i = 0; i < kSlots; ++i) mbar_arrive_expect_tx(smem_u32(&sh->xfull[i]), (uint32_t)(ncta * kStrip * 4));
+        for (int i = 0; i < kSlots; ++i) mbar_arrive_expect_tx(smem_u32(&sh->xfull[i]), (uint32_t)(ncta * 2 * kStrip * 4));
     }
-    if (warp == 13) {
+    if (warp == kCtlW0 + 1) {
         tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 12 && lane == 0) {
+    if (warp == kCtlW0 && lane == 0) {
         prefetch_tmap(&qmap);
         prefetch_tmap(&kmap);
     }
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nld = S / 64;
 
     // (each warpgroup's register change sits in the same branch as the code that uses it)
-    if (warp < 4) {
+    if (warp < kAccW0) {
         // ---------------- exponentials --------------------------------------
         reg_dealloc<kRegsExp>();
         if (nld == 4)
@@ -464,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             exp_role<2>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else
             exp_role<1>(g, sh, err, tmem, xs, ncta, T, c2, nw);
-    } else if (warp < 12) {
+    } else if (warp < kCtlW0) {
         // ---------------- accumulation ---------------------------------------
         reg_alloc<kRegsAcc>();
         if (nld == 4)
@@ -477,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc_role<1>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
     } else {
         reg_dealloc<kRegsCtl>();
-        if (warp == 12) {
+        if (warp == kCtlW0) {
             // ---------------- query strips by TMA ----------------------------------
             int issued = 0;
             for (int j = 0; j < nw; ++j) {
@@ -511,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int gt = max(0, issued - 2); gt < issued; ++gt)
                     wait_phase(smem_u32(&sh->qfull[gt & 1]), (gt >> 1) & 1, sh, err, false);
             __syncwarp();
-        } else if (warp == 14) {
+        } else if (warp == kCtlW0 + 2) {
             // ---------------- key slices by TMA ------------------------------------
             // Window j's key slice goes into buffer j & 1, one TMA box per (paged
             // block, 64-column atom), a block's 16 rows at 16-row steps; a block
@@ -570,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = max(0, kissued - 2); j < kissued; ++j)
                     wait_phase(smem_u32(&sh->kfull[j & 1]), (j >> 1) & 1, sh, err, false);
             __syncwarp();
-        } else if (warp == 13) {
+        } else if (warp == kCtlW0 + 1) {
             // ---------------- MMA issuer -----------------------------------------
             const uint32_t idesc = idesc_bf16(128, S);
             if (lane == 0) {
@@ -623,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
     }
-    if (warp == 13) {
+    if (warp == kCtlW0 + 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
