@@ -387,6 +387,7 @@ def main():
     if args.profile_kernel:
         profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err)
         return
+    groups = kara.kara_batch_groups(c, p, b)
 
     def step(events=None):
         bt.copy_(bt0)                      # every step compresses the same trailing windows
@@ -417,9 +418,10 @@ def main():
         barrier(ws_)
     total_ms = max_over_ranks(t0.elapsed_time(t1), ws_)
     ms = total_ms / args.steps
+    # phases: scoring (every group's); then what the selection, checks, copy and
+    # commit add after it (in groups, most of it ran under the next group's scoring)
     score_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
-    select_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
-    compact_ms = statistics.mean(ev[i][3].elapsed_time(ev[i][4]) for i in range(args.steps))
+    after_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][4]) for i in range(args.steps))
     qring_ms = statistics.mean(ev[i][4].elapsed_time(ev[i][5]) for i in range(args.steps)) if args.q_ring else None
     status = kara.kara_get_error(err)
     if status != 0:
@@ -460,6 +462,7 @@ def main():
             e2e_ms.append(a0.elapsed_time(a1))
     assert int(h_err[0]) == 0
     e2e_ms_v = max_over_ranks(statistics.mean(e2e_ms), ws_)
+    select_ms, compact_ms = standalone_phases(kara, spec, c, p, b, bt, bt0, fresh, freed, new_len, ws, err, stream)
     h2d = (h_len.numel() + h_bt.numel() + h_fresh.numel()) * 4
     d2h = (h_bt_out.numel() + h_len_out.numel() + h_freed.numel() + 1) * 4
 
@@ -492,12 +495,14 @@ def main():
                                f"Top-K {spec.K}, R {spec.R}",
                    "variant": {"score": args.score_mode, "select": args.select_mode, "chunk": args.chunk},
                    "l2": "inputs larger than L2 (Q windows and K/V pools are tens of GB per step)",
-                   "step": "block table restored by a device copy, then kara_compress_batch",
+                   "step": "block table restored by a device copy, then kara_compress_batch"
+                           + (f" (pipelined in {groups} groups of sequences)" if groups > 1 else ""),
                    "parallelism": f"dp{ws_} (independent batches per GPU)"},
         "roofline": roof,
-        "phases_ms": {"score": score_ms, "select": select_ms, "compact_commit": compact_ms,
+        "phases_ms": {"score": score_ms, "after_score": after_ms, "groups": groups,
                       "score_gbs": score_bytes / (score_ms * 1e-3) / 1e9,
-                      "compact_gbs": compact_bytes / (compact_ms * 1e-3) / 1e9},
+                      "select_alone": select_ms, "compact_alone": compact_ms,
+                      "compact_alone_gbs": compact_bytes / (compact_ms * 1e-3) / 1e9},
         "step_roofline": {"t_flop_ms": flops / (tf_burst * 1e12) * 1e3,
                           "t_hbm_ms": (score_bytes + compact_bytes) / (hbm * 1e9) * 1e3,
                           "frac": max(flops / (tf_burst * 1e12), (score_bytes + compact_bytes) / (hbm * 1e9))
@@ -507,7 +512,7 @@ def main():
         "gpu_launches": None,
         "clocks": clocks,
     }
-    line["gpu_launches"] = args.steps * (launches_per_step(spec.W, args.score_mode == "causal")
+    line["gpu_launches"] = args.steps * (launches_per_step(spec.W, args.score_mode == "causal", groups)
                                          + (1 if args.q_ring else 0))
     if args.q_ring:
         qbytes = nwin * spec.G * (spec.R + spec.B) * spec.d * 2 * 2
@@ -708,12 +713,46 @@ def run_serve_sim(args, dev):
         print(json.dumps(line), flush=True)
 
 
-def launches_per_step(W, causal):
+def standalone_phases(kara, spec, c, p, b, bt, bt0, fresh, freed, new_len, ws, err, stream, reps=3):
+    """Selection (kara_select) and checks + compaction + commit (kara_compact)
+    timed through their own entry points on the step's data, outside the timed
+    step: inside kara_compress_batch they overlap the scoring when it runs in
+    groups.  Returns their mean times in ms."""
+    dev = bt.device
+    scores = torch.empty(spec.n_windows, spec.C, dtype=torch.float32, device=dev)
+    cand = torch.empty(spec.n_windows, spec.K, dtype=torch.int32, device=dev)
+    kept = torch.empty(spec.n_windows, spec.R, dtype=torch.int32, device=dev)
+    bt.copy_(bt0)
+    kara.kara_compress_batch(c, p, b, fresh, freed, new_len, ws, err, scores, cand, kept, stream=stream)
+    sel, cmp_ = [], []
+    for _ in range(reps):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        bt.copy_(bt0)
+        e0.record(stream)
+        kara.kara_select(p, spec.n_windows, scores, cand, kept, stream)
+        e1.record(stream)
+        kara.kara_compact(c, p, b, kept, fresh, freed, new_len, err, ws, stream)
+        e2.record(stream)
+        e2.synchronize()
+        sel.append(e0.elapsed_time(e1))
+        cmp_.append(e1.elapsed_time(e2))
+    status = kara.kara_get_error(err)
+    if status != 0:
+        raise SystemExit(f"compaction reported {kara.status_string(status)}")
+    bt.copy_(bt0)
+    torch.cuda.synchronize()
+    return statistics.mean(sel), statistics.mean(cmp_)
+
+
+def launches_per_step(W, causal, groups=1):
     """Kernels of this library per kara_compress_batch: plan, score, select, the
     fresh-id and kept-row checks, compact, commit.  Bidirectional scoring with
     W <= 1024 is the single-pass kernel plus the exact recompute of marked
-    windows (two launches); otherwise the two-pass kernel (one)."""
-    return 6 + (2 if (W <= 1024 and not causal) else 1)
+    windows (two launches); otherwise the two-pass kernel (one).  In groups,
+    each group has its own score, select, kept-check and compact launches;
+    plan, fresh-id check and commit run once."""
+    score = 2 if (W <= 1024 and not causal) else 1
+    return 6 + score if groups <= 1 else 3 + groups * (score + 3)
 
 
 def profile_kernel(args, kara, spec, wl, c, p, b, fresh, freed, new_len, ws, err):

@@ -94,6 +94,13 @@ kara_status geo_from_args(const kara_cache *c, const kara_params *p, const kara_
 cudaError_t launch_plan(const Geo &g, int64_t n_fresh, SeqPlan *plan, int32_t *err, cudaStream_t st);
 cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
                            int64_t n_fresh, int32_t *err, cudaStream_t st);
+// The two halves of launch_compact: the fresh-id check of a whole batch, and the
+// kept-row check plus the copy of a batch or of a group of its sequences (plan
+// then points at the group's first entry; offsets into fresh stay the batch's).
+cudaError_t launch_fresh_check(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int64_t n_fresh,
+                               int32_t *err, cudaStream_t st);
+cudaError_t launch_kept_copy(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
+                             int64_t n_fresh, int32_t *err, cudaStream_t st);
 cudaError_t launch_commit(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int32_t *freed,
                           int32_t *new_len, int32_t *bt, const int32_t *err, cudaStream_t st);
 cudaError_t launch_select(int64_t nwin, int C, int K, int R, float lambda, int mode, int chunk, const float *scores,
@@ -108,5 +115,9 @@ cudaError_t launch_qring_append(const kara_cache *c, const kara_params *p, const
                                 const void *q_new, cudaStream_t st);
 int decode_max_splits(int32_t bt_stride, int32_t block_size);
 cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
+// SMs the single-pass scorer leaves idle on batch g, and its resident clusters
+// (both 0 when the single-pass kernel does not cover g).
+int score_idle_sms(const Geo &g);
+int score_resident_clusters(const Geo &g);
 
 }  // namespace kara

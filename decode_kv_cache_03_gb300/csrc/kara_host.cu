@@ -1,6 +1,7 @@
 // Host side of the C ABI: argument checks, workspace layout and the launch
 // sequence of each entry point.  No allocation, no stream synchronisation
 // (except kara_get_error).
+#include <stdlib.h>
 #include <string.h>
 
 #include <nvtx3/nvToolsExt.h>
@@ -114,6 +115,78 @@ template <class T>
 T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
 
 kara_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KARA_OK : KARA_ECUDA; }
+
+// ---- pipelined batches ------------------------------------------------------
+// The single-pass scorer holds one CTA per SM on the SMs its resident clusters
+// cover and leaves the rest idle (on GB300, 36 clusters of 4 CTAs take 144 of
+// 152 SMs at W = 1024).  A large batch is therefore split into groups of
+// sequences: the scoring of group i + 1 runs while the selection, kept-row check
+// and copy of group i run on a second, lower-priority stream and take the idle
+// SMs.  The fresh-id check of the whole batch runs before any copy and the table
+// commit of the whole batch after every copy, so the call stays all-or-nothing
+// for the tables; each group writes only its own sequences' fresh blocks.  The
+// groups are scored one after another on one stream: while a group's last
+// clusters finish, the queued selection and copy work also takes the SMs they
+// leave (scoring the groups on two alternating streams measured slower, as that
+// work then fell behind on the idle SMs alone).
+constexpr int kMaxGroups = 8;
+constexpr int kMinIdleSms = 4;           // fewer idle SMs: the overlap cannot pay for the groups' tails
+constexpr int kWindowsPerCluster = 32;   // windows each resident cluster scores per group, at least
+
+// Sequences [s0, s1) of a batch as a batch of their own.
+Geo sub_batch(const Geo &g, int s0, int s1)
+{
+    Geo h = g;
+    h.n = s1 - s0;
+    h.len = g.len + s0;
+    h.bt = g.bt + (int64_t)s0 * g.bt_stride;
+    h.q = g.q + (int64_t)s0 * g.layers * g.hq * g.W * g.D;
+    h.nwin = (int64_t)h.n * g.layers * g.hkv;
+    return h;
+}
+
+// Groups of sequences kara_compress_batch splits batch g into (1: none).
+// KARA_BATCH_GROUPS=<m> overrides the choice (clamped to [1, min(n, 64)]).
+static_assert(kMaxGroups <= 64, "events of a pipelined call");
+int batch_groups(const Geo &g)
+{
+    if (g.n < 2) return 1;
+    if (const char *v = getenv("KARA_BATCH_GROUPS")) {
+        const int m = atoi(v);
+        const int cap = g.n < 64 ? g.n : 64;
+        return m < 1 ? 1 : m > cap ? cap : m;
+    }
+    if (score_idle_sms(g) < kMinIdleSms) return 1;
+    const int64_t nres = score_resident_clusters(g);
+    int64_t m = g.nwin / (kWindowsPerCluster * (nres > 0 ? nres : 1));
+    if (m > kMaxGroups) m = kMaxGroups;
+    if (m > g.n) m = g.n;
+    return m < 2 ? 1 : (int)m;
+}
+
+// The streams and events of one pipelined call, released when the call returns
+// (CUDA frees them once the work queued on them has completed).
+struct Pipeline {
+    cudaStream_t score = nullptr, rest = nullptr;
+    cudaEvent_t ev[64 + 3] = {};
+    int nev = 0;
+    ~Pipeline()
+    {
+        for (int i = 0; i < nev; ++i)
+            if (ev[i]) cudaEventDestroy(ev[i]);
+        if (score) cudaStreamDestroy(score);
+        if (rest) cudaStreamDestroy(rest);
+    }
+    cudaError_t init(int nevents)
+    {
+        int least = 0, greatest = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&score, cudaStreamNonBlocking, greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&rest, cudaStreamNonBlocking, least);
+        for (; e == cudaSuccess && nev < nevents; ++nev) e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+        return e;
+    }
+};
 
 }  // namespace
 
@@ -317,6 +390,45 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
     auto mark = [&](int i) -> cudaError_t {
         return phase_events ? cudaEventRecord((cudaEvent_t)phase_events[i], s) : cudaSuccess;
     };
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return KARA_ECUDA;
+    const int m = cap == cudaStreamCaptureStatusNone ? batch_groups(g) : 1;
+    if (m > 1) {
+        // groups of sequences: scoring on a high-priority stream, selection and
+        // copy of each scored group on a low-priority one, both forked from and
+        // joined back to `stream`
+        Pipeline pl;
+        uint8_t *scratch = at<uint8_t>(ws, w.scratch);
+        cudaError_t e = pl.init(m + 2);
+        if (e == cudaSuccess) e = mark(0);
+        if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
+        if (e == cudaSuccess) e = launch_plan(g, n_fresh, plan, err, s);
+        if (e == cudaSuccess) e = launch_fresh_check(g, plan, fresh, n_fresh, err, s);
+        if (e == cudaSuccess) e = mark(1);
+        if (e == cudaSuccess) e = cudaEventRecord(pl.ev[0], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(pl.score, pl.ev[0], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(pl.rest, pl.ev[0], 0);
+        const int64_t wps = (int64_t)g.layers * g.hkv;  // windows per sequence
+        for (int i = 0; i < m && e == cudaSuccess; ++i) {
+            const int s0 = (int)((int64_t)i * g.n / m), s1 = (int)((int64_t)(i + 1) * g.n / m);
+            const Geo gi = sub_batch(g, s0, s1);
+            const int64_t u0 = s0 * wps;
+            e = launch_score(gi, scores + u0 * g.C, scratch + u0, err, pl.score);
+            if (e == cudaSuccess) e = cudaEventRecord(pl.ev[1 + i], pl.score);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(pl.rest, pl.ev[1 + i], 0);
+            if (e == cudaSuccess)
+                e = launch_select(gi.nwin, g.C, g.K, g.R, g.lambda, p->select_mode, p->chunk, scores + u0 * g.C,
+                                  cand + u0 * g.K, kept + u0 * g.R, pl.rest);
+            if (e == cudaSuccess) e = launch_kept_copy(gi, plan + s0, kept + u0 * g.R, fresh, n_fresh, err, pl.rest);
+        }
+        if (e == cudaSuccess && phase_events) e = cudaEventRecord((cudaEvent_t)phase_events[2], pl.score);
+        if (e == cudaSuccess) e = cudaEventRecord(pl.ev[1 + m], pl.rest);  // after every group (rest waited on each)
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, pl.ev[1 + m], 0);
+        if (e == cudaSuccess) e = mark(3);
+        if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);
+        if (e == cudaSuccess) e = mark(4);
+        return cuda_status(e);
+    }
     cudaError_t e = mark(0);
     if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
     if (e == cudaSuccess) e = launch_plan(g, n_fresh, plan, err, s);
@@ -330,6 +442,14 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
     if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);
     if (e == cudaSuccess) e = mark(4);
     return cuda_status(e);
+}
+
+int32_t kara_batch_groups(const kara_cache *c, const kara_params *p, const kara_batch *b)
+{
+    Geo g;
+    const kara_status st = make_geo(c, p, b, &g);
+    if (st != KARA_OK) return (int32_t)st;
+    return batch_groups(g);
 }
 
 kara_status kara_get_error(const int32_t *err, kara_stream_t stream)

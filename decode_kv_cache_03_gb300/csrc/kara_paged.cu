@@ -258,27 +258,41 @@ cudaError_t launch_plan(const Geo &g, int64_t n_fresh, SeqPlan *plan, int32_t *e
     return cudaGetLastError();
 }
 
-// The checks, then the copy (which runs only if no error was recorded).
-cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
-                           int64_t n_fresh, int32_t *err, cudaStream_t st)
+// The fresh-id check of the whole batch (before any copy of any group).
+cudaError_t launch_fresh_check(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int64_t n_fresh,
+                               int32_t *err, cudaStream_t st)
+{
+    if (g.nwin == 0) return cudaSuccess;
+    const int64_t probes = n_fresh + (int64_t)g.n * g.bt_stride;
+    const int64_t per = (int64_t)kChkThreads * kChkProbes;
+    const int64_t nb = (probes + per - 1) / per;
+    if (nb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    fresh_check_kernel<<<(unsigned)nb, kChkThreads, 0, st>>>(g, plan, fresh, n_fresh, err);
+    return cudaGetLastError();
+}
+
+// The kept-row check, then the copy (which runs only if no error was recorded).
+cudaError_t launch_kept_copy(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
+                             int64_t n_fresh, int32_t *err, cudaStream_t st)
 {
     const int64_t blocks = g.nwin * 2;
     if (blocks == 0) return cudaSuccess;
-    {
-        const int64_t probes = n_fresh + (int64_t)g.n * g.bt_stride;
-        const int64_t per = (int64_t)kChkThreads * kChkProbes;
-        const int64_t nb = (probes + per - 1) / per;
-        if (nb > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        fresh_check_kernel<<<(unsigned)nb, kChkThreads, 0, st>>>(g, plan, fresh, n_fresh, err);
-        const int64_t nk = g.nwin * g.R;
-        const int64_t kb = (nk + kChkThreads - 1) / kChkThreads;
-        kept_check_kernel<<<(unsigned)(kb < 4096 ? kb : 4096), kChkThreads, 0, st>>>(nk, g.R, g.C, kept, err);
-    }
+    const int64_t nk = g.nwin * g.R;
+    const int64_t kb = (nk + kChkThreads - 1) / kChkThreads;
+    kept_check_kernel<<<(unsigned)(kb < 4096 ? kb : 4096), kChkThreads, 0, st>>>(nk, g.R, g.C, kept, err);
     if (g.D == 128)
         compact_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(g, plan, kept, fresh, n_fresh, err);
     else
         compact_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(g, plan, kept, fresh, n_fresh, err);
     return cudaGetLastError();
+}
+
+// The checks, then the copy (which runs only if no error was recorded).
+cudaError_t launch_compact(const Geo &g, const SeqPlan *plan, const int32_t *kept, const int32_t *fresh,
+                           int64_t n_fresh, int32_t *err, cudaStream_t st)
+{
+    const cudaError_t e = launch_fresh_check(g, plan, fresh, n_fresh, err, st);
+    return e == cudaSuccess ? launch_kept_copy(g, plan, kept, fresh, n_fresh, err, st) : e;
 }
 
 cudaError_t launch_commit(const Geo &g, const SeqPlan *plan, const int32_t *fresh, int32_t *freed,

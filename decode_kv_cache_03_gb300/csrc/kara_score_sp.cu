@@ -685,6 +685,40 @@ __global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *_
     }
 }
 
+// Clusters of ncta CTAs of the scorer that fit on the device at once (one CTA
+// per SM), from the occupancy query, cached per shape.  Sets the kernel's
+// dynamic shared memory limit, which the query and the launch both need.
+template <int D>
+cudaError_t resident_clusters(int ncta, int *out)
+{
+    auto kern = score_sp_kernel<D>;
+    const size_t smem = smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    static int resident[kMaxCta + 1] = {};
+    int &nres = resident[ncta];
+    if (nres == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.gridDim = dim3((unsigned)ncta);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ncta;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        nres = n;
+    }
+    *out = nres;
+    return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err, cudaStream_t st)
 {
@@ -732,7 +766,8 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
         nreg = fa.numRegs;
     }
     if (nreg != kRegsLaunch) return cudaErrorInvalidKernelImage;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int nres = 0;
+    cudaError_t e = resident_clusters<D>(ncta, &nres);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
@@ -746,16 +781,6 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // one resident cluster per group of ncta SMs; each walks its share of the windows
-    static int resident[2][kMaxCta + 1] = {};
-    int &nres = resident[D == 128][ncta];
-    if (nres == 0) {
-        cfg.gridDim = dim3((unsigned)ncta);
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;
-        nres = n;
-    }
     const int64_t nclus = g.nwin < nres ? g.nwin : nres;
     cfg.gridDim = dim3((unsigned)(nclus * ncta));
     const float c2 = 1.4426950408889634f / sqrtf((float)D);
@@ -773,6 +798,33 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
 
 // The single-pass kernel covers bidirectional scoring with at most kMaxCta key slices.
 bool score_sp_supported(const Geo &g) { return !g.causal && g.W <= kSlice * kMaxCta && g.G * g.W <= kFbMaxGW; }
+
+// SMs the single-pass scorer leaves without a CTA of its own while it runs on
+// batch g (0 when it does not cover g or a query fails): other work can use
+// them meanwhile.
+int score_idle_sms(const Geo &g)
+{
+    if (!score_sp_supported(g) || g.nwin == 0) return 0;
+    const int ncta = (g.W + kSlice - 1) / kSlice;
+    int nres = 0, dev = 0, sms = 0;
+    if ((g.D == 128 ? resident_clusters<128>(ncta, &nres) : resident_clusters<64>(ncta, &nres)) != cudaSuccess)
+        return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    const int64_t used = (g.nwin < nres ? g.nwin : nres) * (int64_t)ncta;
+    return sms > used ? (int)(sms - used) : 0;
+}
+
+// Resident clusters of the single-pass scorer for batch g (0 when it does not cover g).
+int score_resident_clusters(const Geo &g)
+{
+    if (!score_sp_supported(g)) return 0;
+    const int ncta = (g.W + kSlice - 1) / kSlice;
+    int nres = 0;
+    if ((g.D == 128 ? resident_clusters<128>(ncta, &nres) : resident_clusters<64>(ncta, &nres)) != cudaSuccess)
+        return 0;
+    return nres;
+}
 
 // Scratch of the single-pass path: one mark byte per window.
 size_t score_sp_scratch_bytes(const Geo &g) { return g.W <= kSlice * kMaxCta ? align256((size_t)g.nwin) : 0; }

@@ -67,6 +67,7 @@ def _load():
         "kara_compact": ([PC, PP, PB, P, P, I64, P, P, P, P, SZ, P], ctypes.c_int),
         "kara_compress_batch": ([PC, PP, PB, P, I64, P, P, P, P, P, P, SZ, P, P, P], ctypes.c_int),
         "kara_get_error": ([P, P], ctypes.c_int),
+        "kara_batch_groups": ([PC, PP, PB], I32),
         "kara_compact_static": ([PC, PP, PB, P, P, I64, P, P, P, P], ctypes.c_int),
         "kara_decode_workspace_size": ([PC, I32, I32], SZ),
         "kara_compact_queries": ([PC, PP, PB, P, P, P], ctypes.c_int),
@@ -83,7 +84,8 @@ def _load():
 _lib = _load()
 EXPORTED = ("kara_status_string", "kara_version", "kara_plan", "kara_workspace_size", "kara_score",
             "kara_select", "kara_compact", "kara_compress_batch", "kara_get_error", "kara_compact_static",
-            "kara_decode_workspace_size", "kara_decode_attention", "kara_compact_queries", "kara_append_queries")
+            "kara_decode_workspace_size", "kara_decode_attention", "kara_compact_queries", "kara_append_queries",
+            "kara_batch_groups")
 STATIC_MAX_SEQS = 8192     # KARA_STATIC_MAX_SEQS
 
 
@@ -212,6 +214,13 @@ def kara_compress_batch(c: Cache, p: Params, b: Batch, fresh, freed, new_len, ws
                                     int(fresh.numel()), _ptr(freed), _ptr(new_len), _ptr(scores_out),
                                     _ptr(cand_out), _ptr(kept_out), _ptr(ws), ws.numel() * ws.element_size(),
                                     _ptr(err), _stream(stream), ev), "kara_compress_batch")
+
+
+def kara_batch_groups(c: Cache, p: Params, b: Batch) -> int:
+    """Sequence groups kara_compress_batch pipelines this batch into (1: none)."""
+    r = int(_lib.kara_batch_groups(ctypes.byref(c), ctypes.byref(p), ctypes.byref(b)))
+    _check(r if r < 0 else OK, "kara_batch_groups")
+    return r
 
 
 def kara_get_error(err: torch.Tensor, stream=None) -> int:

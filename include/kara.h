@@ -276,18 +276,42 @@ kara_status kara_compact(const kara_cache *c, const kara_params *p, const kara_b
 
 /*
  * The whole step for a batch: zero *err, plan, score, select, compact and
- * commit, all on `stream` without a host synchronisation.  scores_out,
- * cand_out, kept_out may be NULL (then the workspace holds them); when given
- * they receive [n][layers][Hkv][C], [..][K], [..][R].
- * phase_events: NULL, or 5 cudaEvent_t handles (cast to void *) that are
- * recorded on `stream` at the start, after the plan, after scoring, after
- * selection and after compaction + commit, for callers that time the phases.
+ * commit, without a host synchronisation: the work is ordered after what
+ * `stream` already holds, and what is queued on `stream` afterwards runs after
+ * all of it.  scores_out, cand_out, kept_out may be NULL (then the workspace
+ * holds them); when given they receive [n][layers][Hkv][C], [..][K], [..][R].
+ * Large batches are pipelined (kara_batch_groups): the sequences are split into
+ * groups, and the selection and compaction of one group run on a second,
+ * lower-priority stream while the next group is scored on a higher-priority
+ * one; both streams are created for the call, forked from and joined back to
+ * `stream`, and released when the call returns (CUDA frees them once their
+ * work completes).  The fresh-id check covers the whole batch before any block
+ * is written, and the tables are committed for the whole batch after every
+ * copy, only if no error was recorded; a scoring error met in a later group
+ * leaves fresh blocks of earlier groups written, never a live block.  A
+ * stream that is being captured into a graph gets the unpipelined sequence.
+ * phase_events: NULL, or 5 cudaEvent_t handles (cast to void *) recorded at
+ * the start, after the plan, after scoring (the last group's), after
+ * selection (pipelined: once the selection and compaction of every group have
+ * joined `stream`) and after compaction + commit (pipelined: the commit), for
+ * callers that time the phases.
  */
 kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const kara_batch *b,
                                 const int32_t *fresh, int64_t n_fresh, int32_t *freed,
                                 int32_t *new_len, float *scores_out, int32_t *cand_out,
                                 int32_t *kept_out, void *ws, size_t ws_bytes, int32_t *err,
                                 kara_stream_t stream, void *const *phase_events);
+
+/*
+ * Number of sequence groups kara_compress_batch pipelines this batch into (1:
+ * scoring, selection and compaction run one after another), or a negative
+ * status when the arguments are invalid.  Groups are used when the scoring
+ * kernel leaves at least 4 SMs of the current device idle and each of its
+ * resident clusters scores at least 32 windows per group; at most 8 groups,
+ * at most one per sequence.  The environment variable KARA_BATCH_GROUPS=<m>
+ * overrides the choice (clamped to [1, min(n, 64)]).
+ */
+int32_t kara_batch_groups(const kara_cache *c, const kara_params *p, const kara_batch *b);
 
 /* Waits for `stream`, reads *err and returns it as a status (KARA_ECUDA if the
  * copy itself fails). */

@@ -109,6 +109,21 @@ def test_argument_checks_happen_before_any_device_work(kara):
     assert st == kara.EWORKSPACE
 
 
+def test_batch_groups_query(kara, monkeypatch):
+    """kara_batch_groups: argument checks as the entry points, one group for a
+    single sequence, and the KARA_BATCH_GROUPS override clamped to [1, min(n, 64)]
+    (no device is touched on these paths)."""
+    p = kara.params(64, 16, 8, 16, 0.1)
+    bad = kara._lib.kara_batch_groups(ctypes.byref(fake_cache(kara, head_dim=96)), ctypes.byref(p),
+                                      ctypes.byref(kara.Batch(5, 16, 16, 16, 16)))
+    assert bad == kara.EUNSUPPORTED
+    c = fake_cache(kara)
+    assert kara.kara_batch_groups(c, p, kara.Batch(1, 16, 16, 16, 16)) == 1
+    for env, n, want in (("3", 5, 3), ("100", 5, 5), ("100", 90, 64), ("0", 5, 1), ("-2", 5, 1)):
+        monkeypatch.setenv("KARA_BATCH_GROUPS", env)
+        assert kara.kara_batch_groups(c, p, kara.Batch(n, 16, 16, 16, 16)) == want, env
+
+
 def test_workspace_size_grows_with_batch(kara):
     c = fake_cache(kara)
     p = kara.params(64, 16, 8, 16, 0.1)
