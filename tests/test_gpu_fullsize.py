@@ -1,7 +1,9 @@
 """Full-size workloads on the GPU, in the launch configuration the benchmark times.
 
 The whole batch goes through one kara_compress_batch call (and its window-query
-ring through one kara_compact_queries call).  A few windows,
+ring through one kara_compact_queries call); on the Qwen3-14B shape that call
+runs in groups of sequences, the selection and copy of one group under the
+scoring of the next.  A few windows,
 sampled by a seeded generator, are recomputed by the oracle one by one from a
 host copy of their inputs taken before the call; every window and every
 sequence is also checked for properties that hold at any size.
@@ -45,6 +47,9 @@ def test_full_batch(name):
     kept = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.R, dtype=torch.int32, device="cuda")
     ws = torch.empty(kara.kara_workspace_size(c, p, spec.n_seq), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    groups = kara.kara_batch_groups(c, p, b)
+    if name == "qwen3_14b":
+        assert groups > 1      # the scorer's 36 clusters of 4 leave 8 of the 152 SMs idle
     kara.kara_compress_batch(c, p, b, wl.fresh, freed, new_len, ws, err, scores, cand, kept)
     assert kara.kara_get_error(err) == 0
 
