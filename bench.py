@@ -261,10 +261,10 @@ def max_over_ranks(x, ws):
     return float(t.item())
 
 
-def sample_layers(wl, seqs, target_s=12.0):
+def sample_layers(wl, seqs, target_s=12.0, threads=None):
     """Layers of the oracle sample: enough for about target_s seconds of host
     work (timed from a one-layer probe), at most the workload's layer count."""
-    _, dt, _, _ = cpu_oracle_sample(wl, seqs, 1)
+    _, dt, _, _ = cpu_oracle_sample(wl, seqs, 1, threads=threads)
     return max(1, min(wl.spec.layers, int(round(target_s / max(dt, 1e-3)))))
 
 
@@ -277,14 +277,16 @@ def run_reference(args, ws, rank):
     spec = synth.SPECS[args.config]
     seqs = list(range(min(2, spec.n_seq)))
     wl = synth.generate(spec.with_(n_seq=len(seqs)), device="cpu")
-    layers_sample = sample_layers(wl, seqs)
+    # only this rank works, so it takes every host core it may run on (under
+    # torchrun each process starts with OMP_NUM_THREADS=1)
+    thr = len(os.sched_getaffinity(0))
+    layers_sample = sample_layers(wl, seqs, threads=thr)
     for _ in range(args.warmup):
-        cpu_oracle_sample(wl, seqs, layers_sample)
+        cpu_oracle_sample(wl, seqs, layers_sample, threads=thr)
     times = []
     nwin = 0
-    thr = oracle.max_threads()
     for _ in range(args.steps):
-        rate, dt, thr, nwin = cpu_oracle_sample(wl, seqs, layers_sample)
+        rate, dt, thr, nwin = cpu_oracle_sample(wl, seqs, layers_sample, threads=thr)
         times.append(dt)
     t = statistics.median(times)
     val = nwin / t

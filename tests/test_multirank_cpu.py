@@ -83,3 +83,25 @@ def test_two_gloo_ranks_aggregate_host_side():
     # ranks work on different batches
     a, b = synth.generate(_rank_spec(0)), synth.generate(_rank_spec(1))
     assert not torch.equal(a.lengths, b.lengths)
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """bench.py --impl reference launched as the benchmark driver launches N = 2
+    (torchrun, one process per rank, gloo here): rank 0 alone runs the oracle
+    on every host core and prints one JSON line; both ranks exit 0."""
+    import json
+    import subprocess
+    import sys
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
