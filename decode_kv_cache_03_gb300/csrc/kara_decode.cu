@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     float *logit = reinterpret_cast<float *>(dsm + kStages * BB);  // [G][kSplit]
     DecShared *sh = reinterpret_cast<DecShared *>(logit + G * kSplit);
 
-    const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+    const int sp = blockIdx.z, g = blockIdx.x, s = blockIdx.y;
     const int32_t L = a.len[s];
     if (!length_ok(a, L)) {
         if (sp == 0 && g == 0 && threadIdx.x == 0) set_err(err, KARA_EINVAL);
@@ -425,7 +425,9 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     const Stall dbg = debug_stall(kDecTimeoutNs);
     a.stall = dbg.on;
     a.wait_ns = dbg.wait_ns;
-    const dim3 grid((unsigned)a.max_splits, (unsigned)a.hkv, (unsigned)n);
+    // split-major: CTAs past a short sequence's end (they exit at once) come last,
+    // where they take slots the grid's tail leaves idle anyway
+    const dim3 grid((unsigned)a.hkv, (unsigned)n, (unsigned)a.max_splits);
     cudaError_t e = c->head_dim == 128 ? launch_split<128>(a, grid, err, st) : launch_split<64>(a, grid, err, st);
     if (e != cudaSuccess) return e;
     if (c->head_dim == 128)

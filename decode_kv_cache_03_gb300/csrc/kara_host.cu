@@ -327,6 +327,7 @@ kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n,
     if (!aligned16(q)) return KARA_EINVAL;
     if (n > 65535 || c->num_kv_heads > 65535 || c->num_q_heads > 65535) return KARA_EUNSUPPORTED;
     if ((int64_t)bt_stride * c->block_size > 0x7fffffffLL) return KARA_EUNSUPPORTED;
+    if (decode_max_splits(bt_stride, c->block_size) > 65535) return KARA_EUNSUPPORTED;  // grid z
     if (!ws || ws_bytes < decode_workspace_bytes(c, n, bt_stride)) return KARA_EWORKSPACE;
     return cuda_status(launch_decode(c, layer, n, len, block_table, bt_stride, q, out, ws, err,
                                      (cudaStream_t)stream));

@@ -208,7 +208,8 @@ kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const
  * that runs out records KARA_ETIMEOUT (outputs are then unspecified).
  * Layout: each (block, KV head) slice of a pool must be block_size * head_dim
  * contiguous bf16 (rows at stride head_dim), as in the layout above.
- * Supported: the kara_cache shapes above; n <= 65535.
+ * Supported: the kara_cache shapes above; n <= 65535; bt_stride * block_size up to
+ * 65535 * 1024 keys (the key splits of a sequence).
  */
 size_t kara_decode_workspace_size(const kara_cache *c, int32_t n, int32_t bt_stride);
 kara_status kara_decode_attention(const kara_cache *c, int32_t layer, int32_t n, const int32_t *len,
