@@ -400,7 +400,7 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
         // joined back to `stream`
         Pipeline pl;
         uint8_t *scratch = at<uint8_t>(ws, w.scratch);
-        cudaError_t e = pl.init(m + 2);
+        cudaError_t e = pl.init(m + 3);
         if (e == cudaSuccess) e = mark(0);
         if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
         if (e == cudaSuccess) e = launch_plan(g, n_fresh, plan, err, s);
@@ -409,6 +409,7 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
         if (e == cudaSuccess) e = cudaEventRecord(pl.ev[0], s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(pl.score, pl.ev[0], 0);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(pl.rest, pl.ev[0], 0);
+        const bool forked = e == cudaSuccess;
         const int64_t wps = (int64_t)g.layers * g.hkv;  // windows per sequence
         for (int i = 0; i < m && e == cudaSuccess; ++i) {
             const int s0 = (int)((int64_t)i * g.n / m), s1 = (int)((int64_t)(i + 1) * g.n / m);
@@ -423,8 +424,15 @@ kara_status kara_compress_batch(const kara_cache *c, const kara_params *p, const
             if (e == cudaSuccess) e = launch_kept_copy(gi, plan + s0, kept + u0 * g.R, fresh, n_fresh, err, pl.rest);
         }
         if (e == cudaSuccess && phase_events) e = cudaEventRecord((cudaEvent_t)phase_events[2], pl.score);
-        if (e == cudaSuccess) e = cudaEventRecord(pl.ev[1 + m], pl.rest);  // after every group (rest waited on each)
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, pl.ev[1 + m], 0);
+        if (forked) {
+            // both streams join `stream` even after a failed launch, so nothing the
+            // call queued is still running when later work on `stream` starts
+            cudaError_t j = cudaEventRecord(pl.ev[1 + m], pl.rest);  // after every group (rest waited on each)
+            if (j == cudaSuccess) j = cudaStreamWaitEvent(s, pl.ev[1 + m], 0);
+            if (j == cudaSuccess) j = cudaEventRecord(pl.ev[2 + m], pl.score);
+            if (j == cudaSuccess) j = cudaStreamWaitEvent(s, pl.ev[2 + m], 0);
+            if (e == cudaSuccess) e = j;
+        }
         if (e == cudaSuccess) e = mark(3);
         if (e == cudaSuccess) e = launch_commit(g, plan, fresh, freed, new_len, b->block_table, err, s);
         if (e == cudaSuccess) e = mark(4);
