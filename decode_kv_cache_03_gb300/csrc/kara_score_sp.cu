@@ -13,7 +13,7 @@
 // Each logit is computed and exponentiated exactly once:
 //
 //   * One thread-block cluster per window, one CTA per slice of <= 256 window
-//     keys (cluster size ceil(W/256) <= 4).  The key slice comes into shared
+//     keys (cluster size ceil(W/256) <= 8).  The key slice comes into shared
 //     memory by TMA, one 16-row paged block at a time through a 5-D tensor map
 //     over the pool (128-byte swizzled, the tensor core's K-major layout); the
 //     window's first key may sit o rows into its block, so the MMA operand
@@ -29,7 +29,9 @@
 //     mbarrier).  The reference r is common to the cluster: the row position's
 //     log-sum-exp two strips earlier, r + log2(sum z), which every CTA
 //     derives from the same exchanged partials in the same order (two strips
-//     back, that exchange has long completed).  So no pass over the logits
+//     back, that exchange has long completed).  It cancels in e / Z; only the
+//     rounding of a window's first two strips depends on the window the
+//     cluster scored before it.  So no pass over the logits
 //     precedes the exponentials, and the row's normaliser is a plain sum.  A strip whose row total sum_c z_c leaves [2^-88, 2^119] --
 //     where the fp32 exponentials could overflow, or lose terms within 2^-30
 //     of the row maximum -- marks its window, and an exact CUDA-core kernel
@@ -46,9 +48,12 @@
 //     across the four lane quarters through shared memory, in a fixed order.
 //
 // The kernel is persistent: each cluster walks its share of the windows, and
-// the next window's key slice loads into the second key buffer while the
-// current window is scored.  No W x W matrix and no per-row statistic reaches
-// global memory; every score is a deterministic fp32 sum.  Warp roles (640
+// (up to 4 CTAs per cluster) the next window's key slice loads into the second
+// key buffer while the current window is scored; with 5..8 CTAs the exchange
+// slots take that room and a slice loads after the previous window's last MMA.
+// No W x W matrix and no per-row statistic reaches global memory; every score
+// is a deterministic fp32 sum for a given batch (the carried reference makes
+// its last bits depend on the window scored before it by the same cluster).  Warp roles (640
 // threads): warps 0..7 exponentials (two per lane quarter, one per half of the
 // keys), 8..15 accumulation, 16 query-strip TMA, 17 TMEM allocation and MMAs
 // (one lane), 18 key-slice TMA (it also reads the window's length and block ids
@@ -74,7 +79,7 @@ using namespace ptx;
 
 constexpr int kSlice = 256;    // keys per CTA
 constexpr int kStrip = 128;    // query rows per strip
-constexpr int kMaxCta = 4;     // CTAs per cluster: W <= 1024
+constexpr int kMaxCta = 8;     // CTAs per cluster: W <= 2048
 constexpr int kSlots = 4;      // exchange slots (strips in flight between CTAs)
 constexpr int kExpW = 8;       // exponential warps: two per TMEM lane quarter (column halves)
 constexpr int kAcc = 256;      // accumulating threads: two per TMEM lane
@@ -133,15 +138,23 @@ struct Shared {
     int wstat[kWinRing];             // a window's status: 0, KARA_EINVAL or KARA_EBADBLOCK
 };
 
-// Exchange slot: the partial sums of every CTA for each row, one per column half.
-constexpr int kSlotFloats = kMaxCta * 2 * kStrip;
+// An instantiation of the kernel covers clusters of up to MAXC CTAs: 4 (W <=
+// 1024) or 8 (W <= 2048).  Its exchange slot holds the partial sums of MAXC
+// CTAs for each row, one per column half.  Up to 4 CTAs there are two key-slice
+// buffers (the next window's slice loads while the current one is scored);
+// with 8 the larger slots leave room for one, and a window's slice loads after
+// the previous window's last MMA.
+template <int MAXC>
+constexpr int kSlotF = MAXC * 2 * kStrip;
+template <int MAXC>
+constexpr int kKeyBufs = MAXC > 4 ? 1 : 2;
 
-template <int D>
+template <int D, int MAXC>
 size_t smem_bytes()
 {
     using C_ = Cfg<D>;
-    const size_t need = 1024 + 2 * (size_t)C_::kKBytes + 2 * (size_t)C_::kQBytes
-                      + (size_t)kSlots * kSlotFloats * 4 + 4 * kSlice * 4 + sizeof(Shared);
+    const size_t need = 1024 + (size_t)kKeyBufs<MAXC> * C_::kKBytes + 2 * (size_t)C_::kQBytes
+                      + (size_t)kSlots * kSlotF<MAXC> * 4 + 4 * kSlice * 4 + sizeof(Shared);
     // more than half of the SM's shared memory: a second CTA never shares the
     // SM and waits in tcgen05.alloc for the TMEM this persistent one holds
     const size_t floor_ = 120 * 1024;
@@ -179,13 +192,14 @@ __device__ __forceinline__ float fv(uint32_t x) { return __uint_as_float(x); }
 
 // Row total of an exchange slot: the partial sums added in (CTA, half) order,
 // so every CTA of the cluster (and both warp roles) gets the same value.
+template <int MAXC>
 __device__ __forceinline__ float slot_total(const float *xs, int slot, int ncta, int row)
 {
-    float Z = xs[slot * kSlotFloats + row] + xs[slot * kSlotFloats + kStrip + row];
+    float Z = xs[slot * kSlotF<MAXC> + row] + xs[slot * kSlotF<MAXC> + kStrip + row];
 #pragma unroll
-    for (int c = 1; c < kMaxCta; ++c)
+    for (int c = 1; c < MAXC; ++c)
         if (c < ncta)
-            Z += xs[slot * kSlotFloats + (2 * c) * kStrip + row] + xs[slot * kSlotFloats + (2 * c + 1) * kStrip + row];
+            Z += xs[slot * kSlotF<MAXC> + (2 * c) * kStrip + row] + xs[slot * kSlotF<MAXC> + (2 * c + 1) * kStrip + row];
     return Z;
 }
 
@@ -209,7 +223,7 @@ __device__ __forceinline__ void exp8(uint32_t (&v)[8], uint64_t c2p, uint64_t nr
 
 // Exponential warps: two per TMEM lane quarter, a thread per query row of the
 // strip and half (32 * NLD) of the slice's keys.
-template <int NLD>
+template <int NLD, int MAXC>
 __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float *xs,
                                          int ncta, int T, float c2, int nw)
 {
@@ -222,7 +236,8 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
     const uint64_t c2p = pack2(c2, c2);
     const uint32_t xs_u = smem_u32(xs);
     // references of this row position for even and odd strips, the same in every
-    // CTA of the cluster
+    // CTA of the cluster (carried across the cluster's windows: the previous
+    // window's row totals start the next one close to its scale)
     float rr[2] = {0.f, 0.f};
     for (int j = 0; j < nw; ++j) {
         for (int t = 0; t < T; ++t) {
@@ -235,7 +250,7 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                 const int ps = (gt - 2) & (kSlots - 1);
                 if (wait_phase(smem_u32(&sh->xfull[ps]), (uint32_t)((gt - 2) / kSlots) & 1u, sh, err) &&
                     !*(volatile int *)&sh->abort) {
-                    const float Z = slot_total(xs, ps, ncta, row);
+                    const float Z = slot_total<MAXC>(xs, ps, ncta, row);
                     if (in_safe_range(Z)) rr[b] += __log2f(Z);
                 }
             }
@@ -273,7 +288,7 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
             // the row's partial goes out first (it does not depend on the TMEM
             // stores); after a time-out the exchange stops: nothing more is sent
             if (!*(volatile int *)&sh->abort) {
-                const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotFloats + (2 * (int)crank + eh) * kStrip + row);
+                const uint32_t xl = xs_u + 4u * (uint32_t)(slot * kSlotF<MAXC> + (2 * (int)crank + eh) * kStrip + row);
                 const uint32_t xb = smem_u32(&sh->xfull[slot]);
                 for (int c = 0; c < ncta; ++c) st_async_f32(mapa(xl, (uint32_t)c), z, mapa(xb, (uint32_t)c));
             }
@@ -287,7 +302,7 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
 
 // Accumulating warps: two per TMEM lane quarter, a thread per query row of the
 // strip and half (NLD 32-column loads) of the slice's keys.
-template <int NLD>
+template <int NLD, int MAXC>
 __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err, float *__restrict__ scores,
                                          uint8_t *__restrict__ marks, uint32_t tmem, const float *xs, float *red,
                                          int ncta, int T, int nw, int cid, int nclus, int slice0)
@@ -328,7 +343,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
             // arrival on a barrier whose phase is still pending would over-arrive).
             const bool got = wait_phase(smem_u32(&sh->xfull[slot]), (uint32_t)(gt / kSlots) & 1u, sh, err) &&
                              !*(volatile int *)&sh->abort;
-            const float Z = slot_total(xs, slot, ncta, row);
+            const float Z = slot_total<MAXC>(xs, slot, ncta, row);
             // rows past G*W (the tail of the last strip) add nothing; a row total
             // out of the safe range marks the window for the exact recompute
             const bool live = got && t * kStrip + row < GW;
@@ -400,7 +415,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
     }
 }
 
-template <int D>
+template <int D, int MAXC>
 __global__ void __launch_bounds__(kThreads, 1)
     score_sp_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, const Geo g,
                     float *__restrict__ scores, uint8_t *__restrict__ marks, int32_t *err, int ncta, int T, float c2,
@@ -411,9 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *base = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sK = base;                                   // two key buffers
-    uint8_t *sQ = sK + 2 * C_::kKBytes;                   // two query stages
+    constexpr int nkb = kKeyBufs<MAXC>;
+    uint8_t *sQ = sK + nkb * C_::kKBytes;                 // two query stages
     float *xs = reinterpret_cast<float *>(sQ + 2 * C_::kQBytes);
-    float *red = xs + kSlots * kSlotFloats;
+    float *red = xs + kSlots * kSlotF<MAXC>;
     Shared *sh = reinterpret_cast<Shared *>(red + 4 * kSlice);
     const uint32_t sK_u = smem_u32(sK), sQ_u = smem_u32(sQ);
 
@@ -466,24 +482,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- exponentials --------------------------------------
         reg_dealloc<kRegsExp>();
         if (nld == 4)
-            exp_role<4>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<4, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else if (nld == 3)
-            exp_role<3>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<3, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else if (nld == 2)
-            exp_role<2>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<2, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
         else
-            exp_role<1>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<1, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
     } else if (warp < kCtlW0) {
         // ---------------- accumulation ---------------------------------------
         reg_alloc<kRegsAcc>();
         if (nld == 4)
-            acc_role<4>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<4, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else if (nld == 3)
-            acc_role<3>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<3, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else if (nld == 2)
-            acc_role<2>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<2, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else
-            acc_role<1>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<1, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
     } else {
         reg_dealloc<kRegsCtl>();
         if (warp == kCtlW0) {
@@ -549,10 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b0 = ok ? x0 / kBlockRows : 0;
                 const int nblk = ok ? (x0 + S - 1) / kBlockRows - b0 + 1 : 0;
                 const int32_t myblk = lane < nblk ? btr[b0 + lane] : 0;
-                const int kb = j & 1;
+                // buffer kb's use j / nkb waits for the MMAs of its previous use
+                const int kb = j % nkb;
                 int go = 0;
                 if (lane == 0) {
-                    if (j >= 2) wait_phase(smem_u32(&sh->kempty[kb]), ((j - 2) >> 1) & 1, sh, err);
+                    if (j >= nkb) wait_phase(smem_u32(&sh->kempty[kb]), (uint32_t)(j / nkb - 1) & 1u, sh, err);
                     sh->koff[kb] = ok ? x0 % kBlockRows : 0;
                     sh->wstat[j & (kWinRing - 1)] = !ok ? KARA_EINVAL : bad ? KARA_EBADBLOCK : 0;
                     mbar_arrive(smem_u32(&sh->wfull[j & (kWinRing - 1)]));
@@ -576,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (lane == 0 && !stall)
-                for (int j = max(0, kissued - 2); j < kissued; ++j)
-                    wait_phase(smem_u32(&sh->kfull[j & 1]), (j >> 1) & 1, sh, err, false);
+                for (int j = max(0, kissued - nkb); j < kissued; ++j)
+                    wait_phase(smem_u32(&sh->kfull[j % nkb]), (uint32_t)(j / nkb) & 1u, sh, err, false);
             __syncwarp();
         } else if (warp == kCtlW0 + 1) {
             // ---------------- MMA issuer -----------------------------------------
@@ -585,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 bool ok = true;
                 for (int j = 0; j < nw && ok; ++j) {
-                    const int kb = j & 1;
-                    ok = wait_phase(smem_u32(&sh->kfull[kb]), (j >> 1) & 1, sh, err);
+                    const int kb = j % nkb;
+                    ok = wait_phase(smem_u32(&sh->kfull[kb]), (uint32_t)(j / nkb) & 1u, sh, err);
                     // the window's first key sits o rows into the key buffer
                     const int o = *(volatile int *)&sh->koff[kb];
                     for (int t = 0; t < T && ok; ++t) {
@@ -688,11 +705,11 @@ __global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *_
 // Clusters of ncta CTAs of the scorer that fit on the device at once (one CTA
 // per SM), from the occupancy query, cached per shape.  Sets the kernel's
 // dynamic shared memory limit, which the query and the launch both need.
-template <int D>
+template <int D, int MAXC>
 cudaError_t resident_clusters(int ncta, int *out)
 {
-    auto kern = score_sp_kernel<D>;
-    const size_t smem = smem_bytes<D>();
+    auto kern = score_sp_kernel<D, MAXC>;
+    const size_t smem = smem_bytes<D, MAXC>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     static int resident[kMaxCta + 1] = {};
@@ -719,12 +736,12 @@ cudaError_t resident_clusters(int ncta, int *out)
     return cudaSuccess;
 }
 
-template <int D>
+template <int D, int MAXC>
 cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err, cudaStream_t st)
 {
     const int ncta = (g.W + kSlice - 1) / kSlice;
     const int T = (g.G * g.W + kStrip - 1) / kStrip;
-    const size_t smem = smem_bytes<D>();
+    const size_t smem = smem_bytes<D, MAXC>();
     auto fn = tensor_map_encoder();
     if (!fn) return cudaErrorNotSupported;
     // query rows: [n * layers * hq * W][D]
@@ -755,7 +772,7 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
             return cudaErrorInvalidValue;
     }
 
-    auto kern = score_sp_kernel<D>;
+    auto kern = score_sp_kernel<D, MAXC>;
     // the warpgroups' register trade is only safe with the launch count it was sized for
     static int regs[2] = {0, 0};
     int &nreg = regs[D == 128];
@@ -767,7 +784,7 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
     }
     if (nreg != kRegsLaunch) return cudaErrorInvalidKernelImage;
     int nres = 0;
-    cudaError_t e = resident_clusters<D>(ncta, &nres);
+    cudaError_t e = resident_clusters<D, MAXC>(ncta, &nres);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
@@ -799,6 +816,13 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
 // The single-pass kernel covers bidirectional scoring with at most kMaxCta key slices.
 bool score_sp_supported(const Geo &g) { return !g.causal && g.W <= kSlice * kMaxCta && g.G * g.W <= kFbMaxGW; }
 
+// resident_clusters of the instantiation that covers clusters of ncta CTAs.
+static cudaError_t resident_for(int D, int ncta, int *nres)
+{
+    if (ncta <= 4) return D == 128 ? resident_clusters<128, 4>(ncta, nres) : resident_clusters<64, 4>(ncta, nres);
+    return D == 128 ? resident_clusters<128, 8>(ncta, nres) : resident_clusters<64, 8>(ncta, nres);
+}
+
 // SMs the single-pass scorer leaves without a CTA of its own while it runs on
 // batch g (0 when it does not cover g or a query fails): other work can use
 // them meanwhile.
@@ -807,8 +831,7 @@ int score_idle_sms(const Geo &g)
     if (!score_sp_supported(g) || g.nwin == 0) return 0;
     const int ncta = (g.W + kSlice - 1) / kSlice;
     int nres = 0, dev = 0, sms = 0;
-    if ((g.D == 128 ? resident_clusters<128>(ncta, &nres) : resident_clusters<64>(ncta, &nres)) != cudaSuccess)
-        return 0;
+    if (resident_for(g.D, ncta, &nres) != cudaSuccess) return 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
     const int64_t used = (g.nwin < nres ? g.nwin : nres) * (int64_t)ncta;
@@ -821,8 +844,7 @@ int score_resident_clusters(const Geo &g)
     if (!score_sp_supported(g)) return 0;
     const int ncta = (g.W + kSlice - 1) / kSlice;
     int nres = 0;
-    if ((g.D == 128 ? resident_clusters<128>(ncta, &nres) : resident_clusters<64>(ncta, &nres)) != cudaSuccess)
-        return 0;
+    if (resident_for(g.D, ncta, &nres) != cudaSuccess) return 0;
     return nres;
 }
 
@@ -832,7 +854,10 @@ size_t score_sp_scratch_bytes(const Geo &g) { return g.W <= kSlice * kMaxCta ? a
 cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
 {
     uint8_t *marks = static_cast<uint8_t *>(scratch);
-    return g.D == 128 ? launch_sp<128>(g, scores, marks, err, st) : launch_sp<64>(g, scores, marks, err, st);
+    const int ncta = (g.W + kSlice - 1) / kSlice;
+    if (ncta <= 4)
+        return g.D == 128 ? launch_sp<128, 4>(g, scores, marks, err, st) : launch_sp<64, 4>(g, scores, marks, err, st);
+    return g.D == 128 ? launch_sp<128, 8>(g, scores, marks, err, st) : launch_sp<64, 8>(g, scores, marks, err, st);
 }
 
 }  // namespace kara

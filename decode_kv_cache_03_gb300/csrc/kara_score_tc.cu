@@ -663,8 +663,8 @@ cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t 
 cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
 {
     if (g.nwin == 0) return cudaSuccess;
-    // one pass over the logits where the single-pass kernel covers the shape;
-    // the two-pass kernel for the causal ablation and windows above 1024 keys
+    // one pass over the logits where the single-pass kernel covers the shape
+    // (bidirectional, W <= 2048); the two-pass kernel for the causal ablation
     if (score_sp_supported(g)) return launch_score_sp(g, scores, scratch, err, st);
     if (g.G * g.W > 8192) return cudaErrorInvalidValue;
     return g.D == 128 ? launch_tc<128>(g, scores, err, st) : launch_tc<64>(g, scores, err, st);

@@ -117,11 +117,12 @@ def test_score_alone_matches_oracle():
 
 
 SCORE_SHAPES = [
-    # (G, W, B, D): cluster sizes 1..8, partial last key slice, partial last query strip,
-    # CTAs with 0, 1 or 2 compressible tiles, both head dims
+    # (G, W, B, D): cluster sizes 1..8 (W up to 2048 on the single-pass kernel), partial
+    # last key slice, partial last query strip, CTAs with 0, 1 or 2 compressible tiles,
+    # both head dims
     (2, 64, 16, 64), (1, 64, 8, 128), (3, 192, 40, 128), (2, 256, 32, 128), (5, 320, 72, 64),
     (4, 512, 64, 128), (1, 640, 100, 128), (5, 1024, 128, 128), (8, 1024, 300, 64), (4, 2048, 256, 128),
-    (2, 1600, 700, 128),
+    (2, 1600, 700, 128), (3, 1280, 200, 64), (2, 1536, 100, 128), (1, 1792, 300, 128),
 ]
 
 
