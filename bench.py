@@ -748,12 +748,11 @@ def standalone_phases(kara, spec, c, p, b, bt, bt0, fresh, freed, new_len, ws, e
 
 def launches_per_step(W, causal, groups=1):
     """Kernels of this library per kara_compress_batch: plan, score, select, the
-    fresh-id and kept-row checks, compact, commit.  Bidirectional scoring with
-    W <= 1024 is the single-pass kernel plus the exact recompute of marked
-    windows (two launches); otherwise the two-pass kernel (one).  In groups,
-    each group has its own score, select, kept-check and compact launches;
-    plan, fresh-id check and commit run once."""
-    score = 2 if (W <= 1024 and not causal) else 1
+    fresh-id and kept-row checks, compact, commit.  Scoring is the single-pass
+    kernel plus the exact recompute of marked windows (two launches).  In
+    groups, each group has its own score, select, kept-check and compact
+    launches; plan, fresh-id check and commit run once."""
+    score = 2
     return 6 + score if groups <= 1 else 3 + groups * (score + 3)
 
 

@@ -8,7 +8,9 @@
 //     p[h,i,j] = softmax_j( <q_{h,i}, k_j> / sqrt(D) ),  i, j < W, h in group g
 //     s[j]     = sum_h sum_i p[h,i,j],  j < C = W - B
 // The softmax of a query row runs over all W window keys; keys j >= C (the
-// protected buffer) take part in the normalisation but are not scored.
+// protected buffer) take part in the normalisation but are not scored.  The
+// causal ablation (score_mode KARA_SCORE_CAUSAL) runs the same kernel with
+// keys j > i masked out of query i's softmax: their exponentials are 0.
 //
 // Each logit is computed and exponentiated exactly once:
 //
@@ -66,12 +68,28 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "kara_common.cuh"
 #include "kara_sm100.cuh"
 
 namespace kara {
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
 
 namespace {
 
@@ -221,11 +239,27 @@ __device__ __forceinline__ void exp8(uint32_t (&v)[8], uint64_t c2p, uint64_t nr
     }
 }
 
+// exp8 for a chunk that straddles the causal diagonal: value e (key j0 + e) is
+// kept where e <= lim (the key is at or before the row's query) and is 0 past it.
+__device__ __forceinline__ void exp8_masked(uint32_t (&v)[8], uint64_t c2p, uint64_t nrp, uint64_t (&z)[2], int lim)
+{
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint64_t y = fma2(pack2(fv(v[i]), fv(v[i + 1])), c2p, nrp);
+        float y0, y1;
+        unpack2(y, y0, y1);
+        const float e0 = i <= lim ? ex2(y0) : 0.f, e1 = i + 1 <= lim ? ex2(y1) : 0.f;
+        v[i] = __float_as_uint(e0);
+        v[i + 1] = __float_as_uint(e1);
+        z[(i >> 1) & 1] = add2(z[(i >> 1) & 1], pack2(e0, e1));
+    }
+}
+
 // Exponential warps: two per TMEM lane quarter, a thread per query row of the
 // strip and half (32 * NLD) of the slice's keys.
-template <int NLD, int MAXC>
+template <int NLD, int MAXC, bool CAUSAL>
 __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err, uint32_t tmem, const float *xs,
-                                         int ncta, int T, float c2, int nw)
+                                         int ncta, int T, float c2, int nw, int slice0)
 {
     constexpr int NCH = 4 * NLD;  // 8-column chunks of this warp's half
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -261,6 +295,9 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
             tc_fence_after();
             uint64_t z2[2] = {0, 0};
             const uint64_t nrp = pack2(-r, -r);
+            // the row's query position minus this warp's first key in the window
+            // (causal masking only)
+            const int qdiff = CAUSAL ? (t * kStrip + row) % g.W - (slice0 + eh * (32 * NLD)) : 0;
             {
                 // two 8-column register sets: chunk c+1 loads while chunk c is
                 // exponentiated (one tcgen05.wait::ld covers all loads in flight);
@@ -273,7 +310,13 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                     uint32_t(&cur)[8] = (c & 1) ? ub : ua;
                     uint32_t(&nxt)[8] = (c & 1) ? ua : ub;
                     if (c + 1 < NCH) tmem_ld8(ta + 8 * (c + 1), nxt);
-                    exp8(cur, c2p, nrp, z2);
+                    if (CAUSAL) {
+                        // keys after the row's query weigh 0; chunks past every row of
+                        // the warp skip the exponentials
+                        exp8_masked(cur, c2p, nrp, z2, qdiff - 8 * c);
+                    } else {
+                        exp8(cur, c2p, nrp, z2);
+                    }
                     tmem_st8(ta + 8 * c, cur);
                     if (c + 1 < NCH) tmem_wait_ld8(nxt);
                 }
@@ -302,7 +345,7 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
 
 // Accumulating warps: two per TMEM lane quarter, a thread per query row of the
 // strip and half (NLD 32-column loads) of the slice's keys.
-template <int NLD, int MAXC>
+template <int NLD, int MAXC, bool CAUSAL>
 __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err, float *__restrict__ scores,
                                          uint8_t *__restrict__ marks, uint32_t tmem, const float *xs, float *red,
                                          int ncta, int T, int nw, int cid, int nclus, int slice0)
@@ -415,7 +458,7 @@ __device__ __forceinline__ void acc_role(const Geo &g, Shared *sh, int32_t *err,
     }
 }
 
-template <int D, int MAXC>
+template <int D, int MAXC, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     score_sp_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, const Geo g,
                     float *__restrict__ scores, uint8_t *__restrict__ marks, int32_t *err, int ncta, int T, float c2,
@@ -482,24 +525,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- exponentials --------------------------------------
         reg_dealloc<kRegsExp>();
         if (nld == 4)
-            exp_role<4, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<4, MAXC, CAUSAL>(g, sh, err, tmem, xs, ncta, T, c2, nw, slice0);
         else if (nld == 3)
-            exp_role<3, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<3, MAXC, CAUSAL>(g, sh, err, tmem, xs, ncta, T, c2, nw, slice0);
         else if (nld == 2)
-            exp_role<2, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<2, MAXC, CAUSAL>(g, sh, err, tmem, xs, ncta, T, c2, nw, slice0);
         else
-            exp_role<1, MAXC>(g, sh, err, tmem, xs, ncta, T, c2, nw);
+            exp_role<1, MAXC, CAUSAL>(g, sh, err, tmem, xs, ncta, T, c2, nw, slice0);
     } else if (warp < kCtlW0) {
         // ---------------- accumulation ---------------------------------------
         reg_alloc<kRegsAcc>();
         if (nld == 4)
-            acc_role<4, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<4, MAXC, CAUSAL>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else if (nld == 3)
-            acc_role<3, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<3, MAXC, CAUSAL>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else if (nld == 2)
-            acc_role<2, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<2, MAXC, CAUSAL>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
         else
-            acc_role<1, MAXC>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
+            acc_role<1, MAXC, CAUSAL>(g, sh, err, scores, marks, tmem, xs, red, ncta, T, nw, cid, nclus, slice0);
     } else {
         reg_dealloc<kRegsCtl>();
         if (warp == kCtlW0) {
@@ -681,13 +724,15 @@ __global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *_
             for (int d = 0; d < g.D; ++d) acc = fmaf(bf(a[d]), bf(b[d]), acc);
             return acc * sc;
         };
-        // pass 1: per query row, log-sum-exp over all W keys (maximum first)
+        // pass 1: per query row, log-sum-exp over all W keys (maximum first); with
+        // the causal mask, over the keys at or before the row's query position
         for (int r = threadIdx.x; r < GW; r += blockDim.x) {
             const uint16_t *q = qw + (int64_t)r * g.D;
+            const int nk = g.causal ? r % g.W + 1 : g.W;
             float m = -INFINITY;
-            for (int j = 0; j < g.W; ++j) m = fmaxf(m, dot(q, key(j)));
+            for (int j = 0; j < nk; ++j) m = fmaxf(m, dot(q, key(j)));
             float z = 0.f;
-            for (int j = 0; j < g.W; ++j) z += expf(dot(q, key(j)) - m);
+            for (int j = 0; j < nk; ++j) z += expf(dot(q, key(j)) - m);
             lse[r] = m + logf(z);
         }
         __syncthreads();
@@ -695,7 +740,8 @@ __global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *_
         for (int j = threadIdx.x; j < g.C; j += blockDim.x) {
             const uint16_t *k = key(j);
             float acc = 0.f;
-            for (int r = 0; r < GW; ++r) acc += expf(dot(qw + (int64_t)r * g.D, k) - lse[r]);
+            for (int r = 0; r < GW; ++r)
+                if (!g.causal || r % g.W >= j) acc += expf(dot(qw + (int64_t)r * g.D, k) - lse[r]);
             scores[u * g.C + j] = acc;
         }
         __syncthreads();
@@ -705,10 +751,10 @@ __global__ void __launch_bounds__(kFbThreads) exact_kernel(const Geo g, float *_
 // Clusters of ncta CTAs of the scorer that fit on the device at once (one CTA
 // per SM), from the occupancy query, cached per shape.  Sets the kernel's
 // dynamic shared memory limit, which the query and the launch both need.
-template <int D, int MAXC>
+template <int D, int MAXC, bool CAUSAL>
 cudaError_t resident_clusters(int ncta, int *out)
 {
-    auto kern = score_sp_kernel<D, MAXC>;
+    auto kern = score_sp_kernel<D, MAXC, CAUSAL>;
     const size_t smem = smem_bytes<D, MAXC>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -736,7 +782,7 @@ cudaError_t resident_clusters(int ncta, int *out)
     return cudaSuccess;
 }
 
-template <int D, int MAXC>
+template <int D, int MAXC, bool CAUSAL>
 cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err, cudaStream_t st)
 {
     const int ncta = (g.W + kSlice - 1) / kSlice;
@@ -772,7 +818,7 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
             return cudaErrorInvalidValue;
     }
 
-    auto kern = score_sp_kernel<D, MAXC>;
+    auto kern = score_sp_kernel<D, MAXC, CAUSAL>;
     // the warpgroups' register trade is only safe with the launch count it was sized for
     static int regs[2] = {0, 0};
     int &nreg = regs[D == 128];
@@ -784,7 +830,7 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
     }
     if (nreg != kRegsLaunch) return cudaErrorInvalidKernelImage;
     int nres = 0;
-    cudaError_t e = resident_clusters<D, MAXC>(ncta, &nres);
+    cudaError_t e = resident_clusters<D, MAXC, CAUSAL>(ncta, &nres);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
@@ -814,13 +860,14 @@ cudaError_t launch_sp(const Geo &g, float *scores, uint8_t *marks, int32_t *err,
 }  // namespace
 
 // The single-pass kernel covers bidirectional scoring with at most kMaxCta key slices.
-bool score_sp_supported(const Geo &g) { return !g.causal && g.W <= kSlice * kMaxCta && g.G * g.W <= kFbMaxGW; }
+bool score_sp_supported(const Geo &g) { return g.W <= kSlice * kMaxCta && g.G * g.W <= kFbMaxGW; }
 
 // resident_clusters of the instantiation that covers clusters of ncta CTAs.
 static cudaError_t resident_for(int D, int ncta, int *nres)
 {
-    if (ncta <= 4) return D == 128 ? resident_clusters<128, 4>(ncta, nres) : resident_clusters<64, 4>(ncta, nres);
-    return D == 128 ? resident_clusters<128, 8>(ncta, nres) : resident_clusters<64, 8>(ncta, nres);
+    if (ncta <= 4)
+        return D == 128 ? resident_clusters<128, 4, false>(ncta, nres) : resident_clusters<64, 4, false>(ncta, nres);
+    return D == 128 ? resident_clusters<128, 8, false>(ncta, nres) : resident_clusters<64, 8, false>(ncta, nres);
 }
 
 // SMs the single-pass scorer leaves without a CTA of its own while it runs on
@@ -851,13 +898,36 @@ int score_resident_clusters(const Geo &g)
 // Scratch of the single-pass path: one mark byte per window.
 size_t score_sp_scratch_bytes(const Geo &g) { return g.W <= kSlice * kMaxCta ? align256((size_t)g.nwin) : 0; }
 
+// Scratch of the scoring path: one mark byte per window.
+size_t score_scratch_bytes(const Geo &g) { return score_sp_scratch_bytes(g); }
+
+cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st);
+
+// Every shape the entry points accept (W <= 2048, G * W <= 8192, bidirectional
+// or causal) is scored in one pass over the logits.
+cudaError_t launch_score(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
+{
+    if (g.nwin == 0) return cudaSuccess;
+    if (!score_sp_supported(g)) return cudaErrorInvalidValue;
+    return launch_score_sp(g, scores, scratch, err, st);
+}
+
 cudaError_t launch_score_sp(const Geo &g, float *scores, void *scratch, int32_t *err, cudaStream_t st)
 {
     uint8_t *marks = static_cast<uint8_t *>(scratch);
     const int ncta = (g.W + kSlice - 1) / kSlice;
+    if (g.causal) {
+        if (ncta <= 4)
+            return g.D == 128 ? launch_sp<128, 4, true>(g, scores, marks, err, st)
+                              : launch_sp<64, 4, true>(g, scores, marks, err, st);
+        return g.D == 128 ? launch_sp<128, 8, true>(g, scores, marks, err, st)
+                          : launch_sp<64, 8, true>(g, scores, marks, err, st);
+    }
     if (ncta <= 4)
-        return g.D == 128 ? launch_sp<128, 4>(g, scores, marks, err, st) : launch_sp<64, 4>(g, scores, marks, err, st);
-    return g.D == 128 ? launch_sp<128, 8>(g, scores, marks, err, st) : launch_sp<64, 8>(g, scores, marks, err, st);
+        return g.D == 128 ? launch_sp<128, 4, false>(g, scores, marks, err, st)
+                          : launch_sp<64, 4, false>(g, scores, marks, err, st);
+    return g.D == 128 ? launch_sp<128, 8, false>(g, scores, marks, err, st)
+                      : launch_sp<64, 8, false>(g, scores, marks, err, st);
 }
 
 }  // namespace kara

@@ -34,7 +34,7 @@ CASES = {
     "llama_8b_4seq": (small("llama_8b", n_seq=4, layers=2, len_lo=1024, len_hi=2100), 4),
     # uneven groups (1, 1, 2 sequences)
     "sweep_w128": (synth.sweep_spec(4, 128).with_(layers=2), 3),
-    # two-pass scorer (W above the single-pass range)
+    # 8 key slices per window (8-CTA clusters, one key buffer)
     "sweep_w2048": (synth.sweep_spec(2, 2048).with_(layers=1), 2),
     "ragged_g3": (random_spec(77, G=3, hkv=2, W=192, B=40, D=128, n_seq=3, layers=2, K=20, R=50,
                               len_lo=192, len_hi=400), 3),
