@@ -29,11 +29,10 @@
 //     and send their partial sum z = sum e of the row to every CTA of the
 //     cluster with st.async (DSMEM, completing bytes on the receiver's
 //     mbarrier).  The reference r is common to the cluster: the row position's
-//     log-sum-exp two strips earlier, r + log2(sum z), which every CTA
-//     derives from the same exchanged partials in the same order (two strips
-//     back, that exchange has long completed).  It cancels in e / Z; only the
-//     rounding of a window's first two strips depends on the window the
-//     cluster scored before it.  So no pass over the logits
+//     log-sum-exp two strips earlier in the same window (0 for a window's first
+//     two strips), r + log2(sum z), which every CTA derives from the same
+//     exchanged partials in the same order (two strips back, that exchange has
+//     long completed).  It cancels in e / Z.  So no pass over the logits
 //     precedes the exponentials, and the row's normaliser is a plain sum.  A strip whose row total sum_c z_c leaves [2^-88, 2^119] --
 //     where the fp32 exponentials could overflow, or lose terms within 2^-30
 //     of the row maximum -- marks its window, and an exact CUDA-core kernel
@@ -54,8 +53,7 @@
 // key buffer while the current window is scored; with 5..8 CTAs the exchange
 // slots take that room and a slice loads after the previous window's last MMA.
 // No W x W matrix and no per-row statistic reaches global memory; every score
-// is a deterministic fp32 sum for a given batch (the carried reference makes
-// its last bits depend on the window scored before it by the same cluster).  Warp roles (640
+// is a deterministic fp32 sum that depends on its own window only.  Warp roles (640
 // threads): warps 0..7 exponentials (two per lane quarter, one per half of the
 // keys), 8..15 accumulation, 16 query-strip TMA, 17 TMEM allocation and MMAs
 // (one lane), 18 key-slice TMA (it also reads the window's length and block ids
@@ -269,18 +267,19 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const uint64_t c2p = pack2(c2, c2);
     const uint32_t xs_u = smem_u32(xs);
-    // references of this row position for even and odd strips, the same in every
-    // CTA of the cluster (carried across the cluster's windows: the previous
-    // window's row totals start the next one close to its scale)
-    float rr[2] = {0.f, 0.f};
     for (int j = 0; j < nw; ++j) {
+        // references of this row position for even and odd strips, the same in
+        // every CTA of the cluster; 0 for a window's first two strips, so a
+        // window's scores do not depend on the windows scored before it
+        float rr[2] = {0.f, 0.f};
         for (int t = 0; t < T; ++t) {
             const int gt = j * T + t, b = gt & 1, slot = gt & (kSlots - 1);
-            // the row total of strip gt - 2 moves that strip's reference to the
-            // row's log2-sum-exp (an out-of-range total, which marks its window,
-            // or a missing one after a time-out leaves it where it was; once the
-            // CTA has aborted, the slots' phases no longer follow the strips)
-            if (gt > 1) {
+            // the row total of strip gt - 2 of the same window moves that strip's
+            // reference to the row's log2-sum-exp (an out-of-range total, which
+            // marks the window, or a missing one after a time-out leaves it where
+            // it was; once the CTA has aborted, the slots' phases no longer follow
+            // the strips)
+            if (t > 1) {
                 const int ps = (gt - 2) & (kSlots - 1);
                 if (wait_phase(smem_u32(&sh->xfull[ps]), (uint32_t)((gt - 2) / kSlots) & 1u, sh, err) &&
                     !*(volatile int *)&sh->abort) {
