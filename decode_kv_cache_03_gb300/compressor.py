@@ -20,6 +20,7 @@ class Compressor:
         self.params = kara.params(W, B, K, R, lam, score_mode, select_mode, chunk)
         self.err = torch.zeros(1, dtype=torch.int32, device=k.device)
         self._ws = torch.empty(0, dtype=torch.uint8, device=k.device)
+        self._dws = torch.empty(0, dtype=torch.uint8, device=k.device)
 
     def workspace(self, n: int) -> torch.Tensor:
         need = kara.kara_workspace_size(self.cache, self.params, n)
@@ -37,6 +38,16 @@ class Compressor:
         ws = self.workspace(b.n)
         kara.kara_compress_batch(self.cache, self.params, b, fresh, freed, new_len, ws, self.err, scores, cand,
                                  kept, stream)
+
+    def decode(self, layer: int, lengths, block_table, q, out, stream=None):
+        """Enqueue decode attention for one layer over the paged cache.  Called on
+        the same stream right after compress() with its new_len and the table it
+        rewrote in place, it reads the compacted cache with no host round trip."""
+        n, bt_stride = block_table.shape
+        need = kara.kara_decode_workspace_size(self.cache, n, bt_stride)
+        if self._dws.numel() < need:
+            self._dws = torch.empty(need, dtype=torch.uint8, device=self.k.device)
+        kara.kara_decode_attention(self.cache, layer, lengths, block_table, q, out, self._dws, self.err, stream)
 
     def error(self, stream=None) -> int:
         return kara.kara_get_error(self.err, stream)

@@ -75,6 +75,38 @@ def test_decode_reads_the_table_compression_rewrote():
         np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
 
 
+def test_decode_on_device_right_after_compress():
+    """Compress, then decode every layer on the same stream from the device-side
+    new lengths and the table the step rewrote in place (no host step between):
+    the oracle's decode of the oracle's compacted cache."""
+    from decode_kv_cache_03_gb300.compressor import Compressor
+    spec = random_spec(511, G=4, hkv=2, W=256, B=32, D=128, n_seq=3, layers=2, len_lo=600, len_hi=1500, K=16,
+                       R=60, plant="bernoulli")
+    wl = synth.generate(spec)
+    d = to_device(wl)
+    comp = Compressor(d.k, d.v, spec.hq, spec.W, spec.B, spec.K, spec.R, spec.lam)
+    _, _, _, to = comp.plan(wl.lengths, wl.bt_stride)
+    bt = d.block_table.clone()
+    freed = torch.empty(to, dtype=torch.int32, device="cuda")
+    new_len = torch.empty(spec.n_seq, dtype=torch.int32, device="cuda")
+    kept = torch.empty(spec.n_seq, spec.layers, spec.hkv, spec.R, dtype=torch.int32, device="cuda")
+    q = synth.decode_queries(spec, 10).cuda()
+    outs = [torch.full((spec.n_seq, spec.hq, spec.d), float("nan"), device="cuda") for _ in range(spec.layers)]
+    comp.compress(d.lengths, bt, d.q, d.fresh, freed, new_len, kept=kept)
+    for layer in range(spec.layers):
+        comp.decode(layer, new_len, bt, q, outs[layer])
+    assert comp.error() == 0
+    kh = wl.k.view(torch.int16).numpy().view(np.uint16)
+    vh = wl.v.view(torch.int16).numpy().view(np.uint16)
+    st, k2, v2, bt2, _, nl2 = oracle.compact(oracle.shape_of(wl), kh, vh, wl.block_table, wl.lengths,
+                                             kept.cpu().numpy(), wl.fresh)
+    assert st == oracle.OK
+    for layer in range(spec.layers):
+        ref = oracle.decode_attention(oracle.shape_of(wl), layer, q.cpu(), torch.from_numpy(k2.view(np.int16)),
+                                      torch.from_numpy(v2.view(np.int16)), bt2, nl2)
+        np.testing.assert_allclose(outs[layer].cpu().numpy(), ref, atol=ATOL, rtol=RTOL)
+
+
 def test_decode_reports_bad_lengths_and_blocks():
     kara = lib()
     spec = random_spec(511, G=2, hkv=2, W=64, B=16, D=64, n_seq=3, layers=1, len_lo=100, len_hi=200)
