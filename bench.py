@@ -652,7 +652,7 @@ def run_decode(args, dev, kara):
     pk = peaks()[0]
     line = {"metric": "decode attention over the paged cache (HBM GB/s)", "value": gbs, "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "dtype": "bf16 in, f32 math", "data": "synthetic",
+            "dtype": "bf16 in, f32 accumulation", "data": "synthetic",
             "config": {"workload": f"{args.config}, one layer: {n} sequences x {spec.hq} query / {spec.hkv} KV heads, "
                                    f"D {spec.d}, lengths {spec.len_lo}..{spec.len_hi}, {kv_bytes / 1e9:.2f} GB of K/V",
                        "l2": "K/V larger than L2, every block distinct"},

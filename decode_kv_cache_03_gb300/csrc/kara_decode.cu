@@ -10,20 +10,36 @@
 // with K and V read through the block table.  Logits, softmax and sums are
 // fp32 (logits in the log2 domain); the output is fp32.
 //
-// The work is HBM-bound (about 2.5 FLOP per byte of K and V), so it runs on
-// the CUDA cores.  Flash-decoding layout: one CTA per (sequence, KV head,
-// split of kSplit keys).  A producer warp streams the split's K blocks, then
-// its V blocks, into a ring of shared-memory stages with the bulk-copy engine
-// (each (block, KV head) of a pool is one contiguous 16 x D bf16 region), so
-// many blocks are in flight per SM without holding registers.  Four consumer
-// warps take one block each: logits with 8 lanes per key and packed fp32
-// pairs, then the softmax of the split in shared memory, then the weighted
-// sum of V.  A second kernel combines the splits of each (sequence, head) in
-// a fixed order, so the result is deterministic.
+// The work is HBM-bound (about 2.5 FLOP per byte of K and V).  Flash-decoding
+// layout: one CTA per (sequence, KV head, split of kSplit keys).  A producer
+// warp streams the split's K blocks, then its V blocks, into a ring of
+// shared-memory stages by TMA: one (block, KV head) slice of 16 rows per
+// stage, as 64-dim halves in the 128-byte swizzled layout, so many blocks are
+// in flight per SM without holding registers.  Four consumer warps take one
+// block each.  The G query heads of a KV head share every key, so both
+// contractions of a block are small bf16 matrix products on the warp-level
+// tensor-core MMA (m16n8k16, fp32 accumulators), the operands read from the
+// swizzled stage with ldmatrix, free of bank conflicts:
+//   logits   S^T[16 keys][8 heads]  = K_blk[16][D] . Q^T[D][8]
+//   outputs  O^T[D][8 heads]       += V_blk^T[D][16] . P^T[16][8]
+// The weights P are fp32; each enters the second product as the sum of two
+// bf16 terms (hi = rn(p), lo = rn(p - hi)), so its relative error is about
+// 2^-17, as good as the fp32 sums around it.  The tensor cores here only
+// save issue slots: about 4 warp instructions per key instead of 46 on the
+// CUDA cores, which left the consumers, not HBM, as the limit.  Between the
+// two products, the softmax of the split runs in shared memory.  A second
+// kernel combines the splits of each (sequence, head) in a fixed order, so
+// the result is deterministic.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kara_common.cuh"
 #include "kara_sm100.cuh"
 
 namespace kara {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();  // defined beside the scoring kernel
+
 namespace {
 
 constexpr int kSplit = 1024;        // keys per CTA
@@ -31,7 +47,9 @@ constexpr int kBlk = 16;            // tokens per cache block (the supported blo
 constexpr int kBlocks = kSplit / kBlk;
 constexpr int kNC = 4;              // consumer warps
 constexpr int kDecThreads = 32 * (1 + kNC);
-constexpr int kStages = 12;         // ring of (block, head) slices in flight
+constexpr int kStages = 8;          // ring of (block, head) slices in flight
+constexpr int kHalf = kBlk * 64 * 2;  // bytes of one 64-dim half of a slice: 16 swizzled 128-byte rows
+constexpr int kLs = kSplit + 8;     // row stride of the logits (floats): the weight fragments load conflict-free
 constexpr uint64_t kDecTimeoutNs = 1000000000ull;  // 1 s: a stage normally lands in microseconds
 // Blocks go to the consumer warps round-robin and stage waits are by phase
 // parity, which tells only two neighbouring phases apart: a warp may wait for
@@ -40,9 +58,7 @@ constexpr uint64_t kDecTimeoutNs = 1000000000ull;  // 1 s: a stage normally land
 static_assert(kStages % kNC == 0, "each stage is reused by the same consumer warp");
 
 struct DecodeArgs {
-    const uint16_t *k, *v;
-    int64_t layer_off, block_stride, head_stride;
-    int32_t num_blocks, hkv, hq, G, bs;
+    int32_t layer, num_blocks, hkv, hq, G, bs;
     const int32_t *len;
     const int32_t *bt;
     int32_t bt_stride, n, max_splits;
@@ -92,75 +108,79 @@ __device__ bool dwait(uint32_t bar, uint32_t parity, DecShared *sh, int32_t *err
     }
 }
 
-__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ float fold2(uint64_t r)
+// ---- warp-level tensor-core operands -------------------------------------------
+// Four 8x8 bf16 tiles from shared memory; lanes 8i..8i+7 give the row
+// addresses of tile i, which lands in r[i].
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
-    float lo, hi;
-    ptx::unpack2(r, lo, hi);
-    return lo + hi;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
 }
 
-// Weighted sum of one V block into acc: lane owns dims [lane*2*VW, +2*VW),
-// tokens taken in pairs so that one packed FMA uses the weights of two
-// adjacent tokens, (p_t, p_t+1) * (v_t, v_t+1).  MASK: the block is the last
-// one of the split and holds tmax < 16 valid rows; rows past it are zeroed
-// (their bytes are whatever the block held) and their weights are 0.
-template <int D, int G, bool MASK>
-__device__ __forceinline__ void v_block(const uint8_t *blkp, const float *wrow, int tmax, int lane,
-                                        uint64_t (&acc)[G][2 * (D / 64)])
+// The same, each tile transposed on the way.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
 {
-    constexpr int VW = D / 64;  // 32-bit words (bf16 pairs) per row per lane
-#pragma unroll
-    for (int t = 0; t < kBlk; t += 2) {
-        if (MASK && t >= tmax) break;
-        uint32_t w0[VW], w1[VW];
-        if constexpr (VW == 2) {
-            const uint2 a = *reinterpret_cast<const uint2 *>(blkp + t * D * 2 + lane * 8);
-            const uint2 b = *reinterpret_cast<const uint2 *>(blkp + (t + 1) * D * 2 + lane * 8);
-            w0[0] = a.x, w0[1] = a.y, w1[0] = b.x, w1[1] = b.y;
-        } else {
-            w0[0] = *reinterpret_cast<const uint32_t *>(blkp + t * D * 2 + lane * 4);
-            w1[0] = *reinterpret_cast<const uint32_t *>(blkp + (t + 1) * D * 2 + lane * 4);
-        }
-        if (MASK && t + 1 >= tmax)
-#pragma unroll
-            for (int e = 0; e < VW; ++e) w1[e] = 0u;
-        uint64_t vp[2 * VW];
-#pragma unroll
-        for (int e = 0; e < VW; ++e) {
-            vp[2 * e] = ptx::pack2(lo_f(w0[e]), lo_f(w1[e]));
-            vp[2 * e + 1] = ptx::pack2(hi_f(w0[e]), hi_f(w1[e]));
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const uint64_t pp = *reinterpret_cast<const uint64_t *>(wrow + h * kSplit + t);
-#pragma unroll
-            for (int d = 0; d < 2 * VW; ++d) acc[h][d] = ptx::fma2(pp, vp[d], acc[h][d]);
-        }
-    }
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
 }
 
-// Dynamic shared memory: ring[kStages][16][D] bf16, logit[G][kSplit] fp32
+// d += A[16x16] . B[16x8], bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) rounded to nearest-even bf16, lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// p = hi + lo + O(2^-17 p), both bf16 pairs; p - hi is exact in fp32.
+__device__ __forceinline__ void split_bf16x2(float2 p, uint32_t &hi, uint32_t &lo)
+{
+    hi = bf16x2(p.x, p.y);
+    lo = bf16x2(p.x - __uint_as_float(hi << 16), p.y - __uint_as_float(hi & 0xffff0000u));
+}
+
+// Dynamic shared memory: 1 KB of alignment slack, ring[kStages] of slices
+// (each [D/64 halves][16 rows][128 B], 128-byte swizzled), logit[G][kLs] fp32
 // (logits, then weights, then the consumers' partial outputs), DecShared.
-// Three CTAs per SM (128 registers a thread) except for the widest groups,
-// whose queries take too many registers for that.
+// Four CTAs per SM (32 slices in flight) up to G = 5 at D = 128; wider
+// groups' logits leave room for three.
 template <int D, int G>
-constexpr int dec_min_blocks() { return D == 128 && G >= 6 ? 2 : 3; }
+constexpr int dec_min_blocks() { return D == 128 && G >= 6 ? 3 : 4; }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_split_kernel(const DecodeArgs a, int32_t *err)
+constexpr size_t dec_smem_bytes()
+{
+    return 1024 + (size_t)kStages * kBlk * D * 2 + sizeof(float) * G * kLs + sizeof(DecShared);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>())
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeArgs a, int32_t *err)
 {
     constexpr int BB = kBlk * D * 2;  // bytes of one (block, head) slice
-    constexpr int NCH = D / 64;       // 8-dim chunks per lane in the logits (dims c*64 + sub*8 ..)
-    constexpr int VW = D / 64;
-    static_assert(G <= 8, "heads per group");
-    static_assert(kNC * D <= kSplit, "partial outputs fit in the logit area");
-    extern __shared__ __align__(128) uint8_t dsm[];
-    uint8_t *ring = dsm;
-    float *logit = reinterpret_cast<float *>(dsm + kStages * BB);  // [G][kSplit]
-    DecShared *sh = reinterpret_cast<DecShared *>(logit + G * kSplit);
+    constexpr int NH = D / 64;        // 64-dim halves of a row
+    constexpr int KS = D / 16;        // k-steps of the logits = 16-dim tiles of the outputs
+    static_assert(G <= 8, "heads per group: one n8 tile");
+    static_assert(kNC * D <= kLs, "partial outputs fit in the logit area");
+    extern __shared__ uint8_t dsm_raw[];
+    // the swizzle pattern repeats every 1024 bytes and is taken from the address
+    uint8_t *ring = dsm_raw + ((1024u - (ptx::smem_u32(dsm_raw) & 1023u)) & 1023u);
+    float *logit = reinterpret_cast<float *>(ring + kStages * BB);  // [G][kLs]
+    DecShared *sh = reinterpret_cast<DecShared *>(logit + G * kLs);
 
     const int sp = blockIdx.z, g = blockIdx.x, s = blockIdx.y;
     const int32_t L = a.len[s];
@@ -188,7 +208,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     if (warp == 0) {
         // ---------------- producer: K blocks 0..nb-1, then V blocks --------------
         if (lane == 0) {
-            const int64_t head_off = a.layer_off + (int64_t)g * a.head_stride;
+            ptx::prefetch_tmap(&kmap);
+            ptx::prefetch_tmap(&vmap);
             int issued = 0;
             for (int j = 0; j < (a.stall ? 0 : 2 * nb); ++j) {
                 const int st = j % kStages;
@@ -202,8 +223,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
                 } else {
                     sh->bad[st] = 0;
                     ptx::mbar_arrive_expect_tx(fb, BB);
-                    ptx::bulk_load(ptx::smem_u32(ring + st * BB), (j < nb ? a.k : a.v) + head_off + (int64_t)blk * a.block_stride,
-                                   BB, fb);
+                    const CUtensorMap *m = j < nb ? &kmap : &vmap;
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        ptx::tma_load_5d(ptx::smem_u32(ring + st * BB + h * kHalf), m, fb, h * 64, 0, g, blk, a.layer);
                 }
                 issued = j + 1;
             }
@@ -215,72 +238,58 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     }
 
     // ---------------- consumers ----------------------------------------------------
-    const int cw = warp - 1, grp = lane >> 3, sub = lane & 7;
-    const int ctid = threadIdx.x - 32;
+    // MMA fragment coordinates: row group r8 = lane / 4, thread tq = lane % 4.
+    const int cw = warp - 1, ctid = threadIdx.x - 32;
+    const int r8 = lane >> 2, tq = lane & 3;
 
-    // this lane's dims of the G queries (c*64 + sub*8 + [0, 8)), pre-scaled into
-    // the log2 domain, as (even, odd) pairs
-    uint64_t qv[G][NCH][4];
+    // Logits' B operand Q^T[16 dims][8 heads]: head r8, dims 16ks + 2tq + {0, 1}
+    // and + 8; heads past G are zero.
+    uint32_t qb[KS][2];
+    {
+        const uint32_t *qh =
+            reinterpret_cast<const uint32_t *>(a.q + ((int64_t)s * a.hq + g * G + min(r8, G - 1)) * D);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)s * a.hq + g * G + h) * D + c * 64 + sub * 8));
-            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qv[h][c][e] = ptx::pack2(lo_f(w[e]) * a.scale2, hi_f(w[e]) * a.scale2);
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = r8 < G ? __ldg(qh + ks * 8 + tq) : 0u;
+            qb[ks][1] = r8 < G ? __ldg(qh + ks * 8 + 4 + tq) : 0u;
         }
+    }
 
-    // ---- logits: lane group grp takes tokens grp + 4k of the block, 8 lanes per token
+    // ---- logits.  A = K rows of the block: tile i of ldmatrix = (rows 8(i&1).., dims +8(i>>1));
+    // in the swizzled stage, 16-byte chunk c of row t sits at chunk c ^ (t & 7)
+    const int kt = lane & 15, kc = lane >> 4;
     for (int i = cw; i < nb; i += kNC) {
         const int st = i % kStages;
         if (!dwait(ptx::smem_u32(&sh->full[st]), (i / kStages) & 1, sh, err, a.wait_ns)) break;
-        const bool bad = sh->bad[st] != 0;
-        const uint8_t *blkp = ring + st * BB;
-        float dot[4][G];
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        if (sh->bad[st] == 0) {
+            const uint32_t sb = ptx::smem_u32(ring + st * BB) + kt * 128;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int t = grp + 4 * k;
-            uint64_t acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = 0ull;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                const uint4 r = *reinterpret_cast<const uint4 *>(blkp + t * D * 2 + c * 128 + sub * 16);
-                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint64_t kp = ptx::pack2(lo_f(w[e]), hi_f(w[e]));
-#pragma unroll
-                    for (int h = 0; h < G; ++h) acc[h] = ptx::fma2(qv[h][c][e], kp, acc[h]);
-                }
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t af[4];
+                ldsm_x4(sb + (ks >> 2) * kHalf + ((((ks & 3) * 2 + kc) ^ (kt & 7)) << 4), af);
+                mma_16816(c, af, qb[ks][0], qb[ks][1]);
             }
-#pragma unroll
-            for (int h = 0; h < G; ++h) dot[k][h] = fold2(acc[h]);
         }
-        // the block's bytes are in registers: hand the stage back
+        // the MMAs have consumed the block's bytes: hand the stage back
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sh->empty[st]));
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int o = 4; o > 0; o >>= 1) dot[k][h] += __shfl_xor_sync(0xffffffffu, dot[k][h], o);
-        // lane sub = k of the group writes token grp + 4k (a zero row gives logit 0)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int x = i * kBlk + grp + 4 * k;
-            if (sub == k && x < nk)
-#pragma unroll
-                for (int h = 0; h < G; ++h) logit[h * kSplit + x] = bad ? 0.f : dot[k][h];
+        // c = S^T at (key r8, heads 2tq, 2tq+1) and (key r8 + 8, same heads); a zero row gives logit 0
+        const int x = i * kBlk + r8, h0 = 2 * tq;
+        if (h0 < G) {
+            if (x < nk) logit[h0 * kLs + x] = c[0] * a.scale2;
+            if (x + 8 < nk) logit[h0 * kLs + x + 8] = c[2] * a.scale2;
+        }
+        if (h0 + 1 < G) {
+            if (x < nk) logit[(h0 + 1) * kLs + x] = c[1] * a.scale2;
+            if (x + 8 < nk) logit[(h0 + 1) * kLs + x + 8] = c[3] * a.scale2;
         }
     }
     ptx::named_barrier(1, kNC * 32);
 
     // ---- softmax of each head over the split (warp cw: heads cw, cw + kNC) -------
     for (int h = cw; h < G; h += kNC) {
-        float *lr = logit + h * kSplit;
+        float *lr = logit + h * kLs;
         float m = -INFINITY;
         for (int x = lane; x < nk; x += 32) m = fmaxf(m, lr[x]);
 #pragma unroll
@@ -298,21 +307,42 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     }
     ptx::named_barrier(1, kNC * 32);
 
-    // ---- weighted sum of V ----------------------------------------------------------
-    uint64_t acc[G][2 * VW];
+    // ---- weighted sum.  A = V^T (dims x keys) by transposing ldmatrix: tile i =
+    // (keys 8(i>>1).., dims +8(i&1)); B = P^T (keys x heads) from the weights
+    float acc[KS][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int d = 0; d < 2 * VW; ++d) acc[h][d] = 0ull;
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+    const int vt = (lane & 7) + ((lane >> 4) << 3), vc = (lane >> 3) & 1;
     for (int i = cw; i < nb; i += kNC) {
         const int j = nb + i, st = j % kStages;
         if (!dwait(ptx::smem_u32(&sh->full[st]), (j / kStages) & 1, sh, err, a.wait_ns)) break;
         if (sh->bad[st] == 0) {
+            // weights of head r8 for keys 2tq, 2tq+1 and 2tq+8, 2tq+9 of the block, as bf16 hi + lo
+            uint32_t bh0 = 0u, bl0 = 0u, bh1 = 0u, bl1 = 0u;
+            if (r8 < G) {
+                const float *w = logit + r8 * kLs + i * kBlk + 2 * tq;
+                split_bf16x2(*reinterpret_cast<const float2 *>(w), bh0, bl0);
+                split_bf16x2(*reinterpret_cast<const float2 *>(w + 8), bh1, bl1);
+            }
+            // rows of the last block past the end hold whatever the block held
+            // (NaN included): their halves of the fragments are zeroed
             const int tmax = min(kBlk, nk - i * kBlk);
-            if (tmax == kBlk)
-                v_block<D, G, false>(ring + st * BB, logit + i * kBlk, tmax, lane, acc);
-            else
-                v_block<D, G, true>(ring + st * BB, logit + i * kBlk, tmax, lane, acc);
+            uint32_t m_lo = 0xffffffffu, m_hi = 0xffffffffu;
+            if (tmax < kBlk) {
+                m_lo = (2 * tq < tmax ? 0x0000ffffu : 0u) | (2 * tq + 1 < tmax ? 0xffff0000u : 0u);
+                m_hi = (2 * tq + 8 < tmax ? 0x0000ffffu : 0u) | (2 * tq + 9 < tmax ? 0xffff0000u : 0u);
+            }
+            const uint32_t sb = ptx::smem_u32(ring + st * BB) + vt * 128;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t af[4];
+                ldsm_x4_t(sb + (mt >> 2) * kHalf + ((((mt & 3) * 2 + vc) ^ (vt & 7)) << 4), af);
+                af[0] &= m_lo, af[1] &= m_lo, af[2] &= m_hi, af[3] &= m_hi;
+                mma_16816(acc[mt], af, bh0, bh1);
+                mma_16816(acc[mt], af, bl0, bl1);
+            }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sh->empty[st]));
@@ -321,10 +351,21 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>()) decode_sp
     // outputs red[kNC][G][D], summed below over the warps in a fixed order
     ptx::named_barrier(1, kNC * 32);
     float *red = logit;
+    {
+        const int h0 = 2 * tq;
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int d = 0; d < 2 * VW; ++d) red[(cw * G + h) * D + lane * 2 * VW + d] = fold2(acc[h][d]);
+        for (int mt = 0; mt < KS; ++mt) {
+            const int d = mt * 16 + r8;  // acc[mt] = O^T at (dims d, d + 8; heads h0, h0 + 1)
+            if (h0 < G) {
+                red[(cw * G + h0) * D + d] = acc[mt][0];
+                red[(cw * G + h0) * D + d + 8] = acc[mt][2];
+            }
+            if (h0 + 1 < G) {
+                red[(cw * G + h0 + 1) * D + d] = acc[mt][1];
+                red[(cw * G + h0 + 1) * D + d + 8] = acc[mt][3];
+            }
+        }
+    }
     ptx::named_barrier(1, kNC * 32);
     for (int x = ctid; x < G * D; x += kNC * 32) {
         const int h = x / D, d = x % D;
@@ -362,29 +403,50 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a)
     o[d] = num / den;
 }
 
-template <int D, int G>
-cudaError_t launch_split_g(const DecodeArgs &a, dim3 grid, int32_t *err, cudaStream_t st)
+// Tensor map over one pool, (d, slot, kv head, block, layer) with the cache's
+// strides; a box is one 64-dim half of a (block, head) slice, 128-byte swizzled.
+cudaError_t pool_map(CUtensorMap *m, const void *pool, const kara_cache *c)
 {
-    const size_t smem = (size_t)kStages * kBlk * D * 2 + sizeof(float) * G * kSplit + sizeof(DecShared);
+    auto fn = tensor_map_encoder();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[5] = {(cuuint64_t)c->head_dim, (cuuint64_t)kBlk, (cuuint64_t)c->num_kv_heads,
+                          (cuuint64_t)c->num_blocks, (cuuint64_t)c->num_layers};
+    cuuint64_t strides[4] = {(cuuint64_t)c->head_dim * 2, (cuuint64_t)c->head_stride * 2,
+                             (cuuint64_t)c->block_stride * 2, (cuuint64_t)c->layer_stride * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)kBlk, 1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+template <int D, int G>
+cudaError_t launch_split_g(const CUtensorMap &km, const CUtensorMap &vm, const DecodeArgs &a, dim3 grid,
+                           int32_t *err, cudaStream_t st)
+{
+    const size_t smem = dec_smem_bytes<D, G>();
     auto kern = decode_split_kernel<D, G>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecThreads, smem, st>>>(a, err);
+    kern<<<grid, kDecThreads, smem, st>>>(km, vm, a, err);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_split(const DecodeArgs &a, dim3 grid, int32_t *err, cudaStream_t st)
+cudaError_t launch_split(const CUtensorMap &km, const CUtensorMap &vm, const DecodeArgs &a, dim3 grid, int32_t *err,
+                         cudaStream_t st)
 {
     switch (a.G) {
-        case 1: return launch_split_g<D, 1>(a, grid, err, st);
-        case 2: return launch_split_g<D, 2>(a, grid, err, st);
-        case 3: return launch_split_g<D, 3>(a, grid, err, st);
-        case 4: return launch_split_g<D, 4>(a, grid, err, st);
-        case 5: return launch_split_g<D, 5>(a, grid, err, st);
-        case 6: return launch_split_g<D, 6>(a, grid, err, st);
-        case 7: return launch_split_g<D, 7>(a, grid, err, st);
-        case 8: return launch_split_g<D, 8>(a, grid, err, st);
+        case 1: return launch_split_g<D, 1>(km, vm, a, grid, err, st);
+        case 2: return launch_split_g<D, 2>(km, vm, a, grid, err, st);
+        case 3: return launch_split_g<D, 3>(km, vm, a, grid, err, st);
+        case 4: return launch_split_g<D, 4>(km, vm, a, grid, err, st);
+        case 5: return launch_split_g<D, 5>(km, vm, a, grid, err, st);
+        case 6: return launch_split_g<D, 6>(km, vm, a, grid, err, st);
+        case 7: return launch_split_g<D, 7>(km, vm, a, grid, err, st);
+        case 8: return launch_split_g<D, 8>(km, vm, a, grid, err, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -400,12 +462,12 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
                           int32_t bt_stride, const void *q, float *out, void *ws, int32_t *err, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
+    CUtensorMap km, vm;
+    cudaError_t e = pool_map(&km, c->k, c);
+    if (e == cudaSuccess) e = pool_map(&vm, c->v, c);
+    if (e != cudaSuccess) return e;
     DecodeArgs a;
-    a.k = static_cast<const uint16_t *>(c->k);
-    a.v = static_cast<const uint16_t *>(c->v);
-    a.layer_off = (int64_t)layer * c->layer_stride;
-    a.block_stride = c->block_stride;
-    a.head_stride = c->head_stride;
+    a.layer = layer;
     a.num_blocks = c->num_blocks;
     a.hkv = c->num_kv_heads;
     a.hq = c->num_q_heads;
@@ -428,7 +490,7 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     // split-major: CTAs past a short sequence's end (they exit at once) come last,
     // where they take slots the grid's tail leaves idle anyway
     const dim3 grid((unsigned)a.hkv, (unsigned)n, (unsigned)a.max_splits);
-    cudaError_t e = c->head_dim == 128 ? launch_split<128>(a, grid, err, st) : launch_split<64>(a, grid, err, st);
+    e = c->head_dim == 128 ? launch_split<128>(km, vm, a, grid, err, st) : launch_split<64>(km, vm, a, grid, err, st);
     if (e != cudaSuccess) return e;
     if (c->head_dim == 128)
         decode_combine_kernel<128><<<dim3((unsigned)a.hq, (unsigned)n), 128, 0, st>>>(a);

@@ -196,7 +196,9 @@ kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const
  * each of n sequences and each query head h (KV head g = h / G):
  *     out[s][h] = sum_{x < len[s]} softmax_x(<q[s][h], k_x> / sqrt(D)) v_x
  * over the keys of layer `layer`, k_x and v_x at logical position x read
- * through block_table.  fp32 logits, softmax and sums; fp32 output.
+ * through block_table.  Logits are sums of exact bf16 products in fp32; the
+ * softmax is fp32; each fp32 weight enters the weighted sum of V as two bf16
+ * terms (relative error about 2^-17) with fp32 accumulation; fp32 output.
  * len [n] (device); block_table [n][bt_stride] (device); q: bf16
  * [n][num_q_heads][head_dim] (device, 16-byte aligned); out: float
  * [n][num_q_heads][head_dim] (device).
@@ -206,6 +208,8 @@ kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const
  * records KARA_EBADBLOCK (the row is read as zeros, never from outside the pool);
  * K/V slices are staged through shared memory behind bounded waits, and one
  * that runs out records KARA_ETIMEOUT (outputs are then unspecified).
+ * Returns KARA_ECUDA, before any launch, if the TMA tensor map over a pool
+ * cannot be encoded (a stride of 2^40 bytes or more, for one).
  * Layout: each (block, KV head) slice of a pool must be block_size * head_dim
  * contiguous bf16 (rows at stride head_dim), as in the layout above.
  * Supported: the kara_cache shapes above; n <= 65535; bt_stride * block_size up to

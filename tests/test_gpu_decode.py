@@ -1,10 +1,11 @@
 """GPU parity of decode attention over the paged cache against the oracle,
 including the cache a compression call has just rewritten.
 
-Tolerance: the logits are fp32 dot products of exact bf16 products (relative
-error about D * 2^-24) and the weighted sums are fp32 over at most a few
-thousand rows, so for unit-scale V the output is within 1e-4 absolute of the
-fp64 result; the test allows 2e-4 absolute plus 1e-3 relative."""
+Tolerance: the logits are fp32 sums of exact bf16 products (relative error
+about D * 2^-24); each weight enters the weighted sum as two bf16 terms
+(relative error about 2^-17) and the sums are fp32 over at most a few thousand
+rows, so for unit-scale V the output is within 1e-4 absolute of the fp64
+result; the test allows 2e-4 absolute plus 1e-3 relative."""
 import numpy as np
 import pytest
 import torch
