@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "compressed windows/sec (seq·layer·kv-head), HBM GB/s, % of roofline"
+# ex2 results per clock per SM that the special-function pipe can deliver: the
+# scoring kernel's ncu capture executes 13.2 ex2 per clock per SM with that pipe
+# at 42.4 % of its peak instruction rate, which puts the peak near 32.
+EXP_PER_CLK_SM = 32
 
 
 def peaks():
@@ -40,6 +44,22 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def exp_diagnostic(spec, nwin, causal, score_ms, mhz, n_sm):
+    """The exponential unit as a third bound of the scorer, reported beside the
+    contract's two: one exponential per (head, query, key) of every window (the
+    causal mask leaves W(W+1)/2 pairs per head), the time they take at the
+    pipe's peak rate on n_sm SMs at mhz, and the rate the scorer reached."""
+    pairs = spec.W * (spec.W + 1) // 2 if causal else spec.W * spec.W
+    count = nwin * spec.G * pairs
+    out = {"count": count, "peak_per_clk_per_sm": EXP_PER_CLK_SM, "sms": n_sm, "t_ms": None,
+           "achieved_per_clk_per_sm": None}
+    if mhz:
+        hz = n_sm * mhz * 1e6
+        out["t_ms"] = count / (EXP_PER_CLK_SM * hz) * 1e3
+        out["achieved_per_clk_per_sm"] = count / (score_ms * 1e-3) / hz
+    return out
 
 
 def measured_traffic(nwin):
@@ -508,7 +528,10 @@ def main():
         "step_roofline": {"t_flop_ms": flops / (tf_burst * 1e12) * 1e3,
                           "t_hbm_ms": (score_bytes + compact_bytes) / (hbm * 1e9) * 1e3,
                           "frac": max(flops / (tf_burst * 1e12), (score_bytes + compact_bytes) / (hbm * 1e9))
-                          / (ms * 1e-3)},
+                          / (ms * 1e-3),
+                          "exp": exp_diagnostic(spec, nwin, args.score_mode == "causal", score_ms,
+                                                clocks.get("sm_mhz") or clocks.get("sm_max_mhz"),
+                                                torch.cuda.get_device_properties(dev).multi_processor_count)},
         "e2e": {"value": nwin * ws_ / (e2e_ms_v * 1e-3), "unit": "windows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": None,

@@ -53,3 +53,19 @@ def test_reference_arm_under_two_ranks():
         assert p.returncode == 0, err[-2000:]
     assert len(_lines(outs[0][0])) == 1 and _lines(outs[0][0])[0]["n_gpus"] == 2
     assert _lines(outs[1][0]) == []
+
+
+def test_exp_diagnostic_counts():
+    """The exponential-unit diagnostic: G*W^2 exponentials per window (W(W+1)/2
+    pairs per head under the causal mask) and their time at the peak rate."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    spec = synth.SPECS["qwen3_14b"]
+    d = bench.exp_diagnostic(spec, spec.n_windows, False, 64.0, 2000.0, 100)
+    assert d["count"] == 40960 * 5 * 1024 * 1024
+    hz = 100 * 2000e6
+    assert d["t_ms"] == pytest.approx(d["count"] / (bench.EXP_PER_CLK_SM * hz) * 1e3)
+    assert d["achieved_per_clk_per_sm"] == pytest.approx(d["count"] / 64e-3 / hz)
+    c = bench.exp_diagnostic(spec, 3, True, 1.0, None, 100)
+    assert c["count"] == 3 * 5 * (1024 * 1025 // 2) and c["t_ms"] is None
