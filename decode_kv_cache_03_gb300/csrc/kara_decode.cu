@@ -33,6 +33,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "kara_common.cuh"
 #include "kara_sm100.cuh"
 
@@ -422,14 +424,60 @@ cudaError_t pool_map(CUtensorMap *m, const void *pool, const kara_cache *c)
     return cudaSuccess;
 }
 
+// A tensor map depends only on the pool's address, shape and strides: each host
+// thread keeps the last pair it encoded, so a decode loop over the layers of one
+// cache encodes them once.
+struct PoolMaps {
+    CUtensorMap km, vm;
+    const void *k, *v;
+    int64_t layer_stride, block_stride, head_stride;
+    int32_t num_layers, num_blocks, num_kv_heads, head_dim;
+    bool valid;
+};
+
+bool same_pools(const PoolMaps &m, const kara_cache *c)
+{
+    return m.valid && m.k == c->k && m.v == c->v && m.layer_stride == c->layer_stride &&
+           m.block_stride == c->block_stride && m.head_stride == c->head_stride && m.num_layers == c->num_layers &&
+           m.num_blocks == c->num_blocks && m.num_kv_heads == c->num_kv_heads && m.head_dim == c->head_dim;
+}
+
+cudaError_t pool_maps(const kara_cache *c, const CUtensorMap **km, const CUtensorMap **vm)
+{
+    thread_local PoolMaps m{};
+    if (!same_pools(m, c)) {
+        m.valid = false;
+        cudaError_t e = pool_map(&m.km, c->k, c);
+        if (e == cudaSuccess) e = pool_map(&m.vm, c->v, c);
+        if (e != cudaSuccess) return e;
+        m.k = c->k, m.v = c->v;
+        m.layer_stride = c->layer_stride, m.block_stride = c->block_stride, m.head_stride = c->head_stride;
+        m.num_layers = c->num_layers, m.num_blocks = c->num_blocks, m.num_kv_heads = c->num_kv_heads;
+        m.head_dim = c->head_dim;
+        m.valid = true;
+    }
+    *km = &m.km;
+    *vm = &m.vm;
+    return cudaSuccess;
+}
+
 template <int D, int G>
 cudaError_t launch_split_g(const CUtensorMap &km, const CUtensorMap &vm, const DecodeArgs &a, dim3 grid,
                            int32_t *err, cudaStream_t st)
 {
     const size_t smem = dec_smem_bytes<D, G>();
     auto kern = decode_split_kernel<D, G>;
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the shared-memory limit is set once per device (bit d of the mask)
+    static std::atomic<uint64_t> set_on{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!(set_on.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        set_on.fetch_or(bit, std::memory_order_release);
+    }
     kern<<<grid, kDecThreads, smem, st>>>(km, vm, a, err);
     return cudaGetLastError();
 }
@@ -462,9 +510,8 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
                           int32_t bt_stride, const void *q, float *out, void *ws, int32_t *err, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
-    CUtensorMap km, vm;
-    cudaError_t e = pool_map(&km, c->k, c);
-    if (e == cudaSuccess) e = pool_map(&vm, c->v, c);
+    const CUtensorMap *km, *vm;
+    cudaError_t e = pool_maps(c, &km, &vm);
     if (e != cudaSuccess) return e;
     DecodeArgs a;
     a.layer = layer;
@@ -490,7 +537,7 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     // split-major: CTAs past a short sequence's end (they exit at once) come last,
     // where they take slots the grid's tail leaves idle anyway
     const dim3 grid((unsigned)a.hkv, (unsigned)n, (unsigned)a.max_splits);
-    e = c->head_dim == 128 ? launch_split<128>(km, vm, a, grid, err, st) : launch_split<64>(km, vm, a, grid, err, st);
+    e = c->head_dim == 128 ? launch_split<128>(*km, *vm, a, grid, err, st) : launch_split<64>(*km, *vm, a, grid, err, st);
     if (e != cudaSuccess) return e;
     if (c->head_dim == 128)
         decode_combine_kernel<128><<<dim3((unsigned)a.hq, (unsigned)n), 128, 0, st>>>(a);

@@ -234,7 +234,10 @@ def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
     planted_q = spec.plant in ("count", "bernoulli", "spans")
     for s in range(n):
         Ls = int(lengths[s])
-        pos = torch.arange(Ls - W, Ls, device=dev)
+        # a sequence shorter than the window (decode-only workloads) holds only
+        # the window's last Ls positions; the draws below stay a full window's
+        first = max(W - Ls, 0)
+        pos = torch.arange(Ls - W + first, Ls, device=dev)
         blk = bt_dev[s, pos // bs].long()
         slot = pos % bs
         kw = torch.randn(Lyr, Hk, W, D, generator=gen, device=dev)
@@ -246,7 +249,7 @@ def generate(spec: Spec, device="cpu", alias_prefix: bool | None = None,
         elif spec.plant != "none":
             m = _plant_mask(spec, gen, dev)
             kw = kw + 3.0 * m[..., None] * u[:, :, None, :]
-        k[:, blk, :, slot, :] = kw.permute(2, 0, 1, 3).to(torch.bfloat16)
+        k[:, blk, :, slot, :] = kw[:, :, first:].permute(2, 0, 1, 3).to(torch.bfloat16)
         if not with_q:
             continue
         qs = torch.randn(Lyr, Hq, W, D, generator=gen, device=dev)
