@@ -33,7 +33,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "kara_common.cuh"
 #include "kara_sm100.cuh"
@@ -424,9 +424,9 @@ cudaError_t pool_map(CUtensorMap *m, const void *pool, const kara_cache *c)
     return cudaSuccess;
 }
 
-// A tensor map depends only on the pool's address, shape and strides: each host
-// thread keeps the last pair it encoded, so a decode loop over the layers of one
-// cache encodes them once.
+// A tensor map depends only on the pool's address, shape and strides: the
+// library keeps the last pair it encoded (static storage, under a lock), so a
+// decode loop over the layers of one cache encodes them once.
 struct PoolMaps {
     CUtensorMap km, vm;
     const void *k, *v;
@@ -442,9 +442,11 @@ bool same_pools(const PoolMaps &m, const kara_cache *c)
            m.num_blocks == c->num_blocks && m.num_kv_heads == c->num_kv_heads && m.head_dim == c->head_dim;
 }
 
-cudaError_t pool_maps(const kara_cache *c, const CUtensorMap **km, const CUtensorMap **vm)
+cudaError_t pool_maps(const kara_cache *c, CUtensorMap *km, CUtensorMap *vm)
 {
-    thread_local PoolMaps m{};
+    static std::mutex mu;
+    static PoolMaps m{};
+    std::lock_guard<std::mutex> lock(mu);
     if (!same_pools(m, c)) {
         m.valid = false;
         cudaError_t e = pool_map(&m.km, c->k, c);
@@ -456,8 +458,8 @@ cudaError_t pool_maps(const kara_cache *c, const CUtensorMap **km, const CUtenso
         m.head_dim = c->head_dim;
         m.valid = true;
     }
-    *km = &m.km;
-    *vm = &m.vm;
+    *km = m.km;
+    *vm = m.vm;
     return cudaSuccess;
 }
 
@@ -467,17 +469,8 @@ cudaError_t launch_split_g(const CUtensorMap &km, const CUtensorMap &vm, const D
 {
     const size_t smem = dec_smem_bytes<D, G>();
     auto kern = decode_split_kernel<D, G>;
-    // the shared-memory limit is set once per device (bit d of the mask)
-    static std::atomic<uint64_t> set_on{0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
-    if (!(set_on.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        set_on.fetch_or(bit, std::memory_order_release);
-    }
     kern<<<grid, kDecThreads, smem, st>>>(km, vm, a, err);
     return cudaGetLastError();
 }
@@ -510,7 +503,7 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
                           int32_t bt_stride, const void *q, float *out, void *ws, int32_t *err, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
-    const CUtensorMap *km, *vm;
+    CUtensorMap km, vm;
     cudaError_t e = pool_maps(c, &km, &vm);
     if (e != cudaSuccess) return e;
     DecodeArgs a;
@@ -537,7 +530,7 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     // split-major: CTAs past a short sequence's end (they exit at once) come last,
     // where they take slots the grid's tail leaves idle anyway
     const dim3 grid((unsigned)a.hkv, (unsigned)n, (unsigned)a.max_splits);
-    e = c->head_dim == 128 ? launch_split<128>(*km, *vm, a, grid, err, st) : launch_split<64>(*km, *vm, a, grid, err, st);
+    e = c->head_dim == 128 ? launch_split<128>(km, vm, a, grid, err, st) : launch_split<64>(km, vm, a, grid, err, st);
     if (e != cudaSuccess) return e;
     if (c->head_dim == 128)
         decode_combine_kernel<128><<<dim3((unsigned)a.hq, (unsigned)n), 128, 0, st>>>(a);
