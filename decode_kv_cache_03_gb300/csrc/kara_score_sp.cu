@@ -310,8 +310,8 @@ __device__ __forceinline__ void exp_role(const Geo &g, Shared *sh, int32_t *err,
                     uint32_t(&nxt)[8] = (c & 1) ? ua : ub;
                     if (c + 1 < NCH) tmem_ld8(ta + 8 * (c + 1), nxt);
                     if (CAUSAL) {
-                        // keys after the row's query weigh 0; chunks past every row of
-                        // the warp skip the exponentials
+                        // keys after the row's query weigh 0 (a select per element,
+                        // cheaper than branching on the chunk)
                         exp8_masked(cur, c2p, nrp, z2, qdiff - 8 * c);
                     } else {
                         exp8(cur, c2p, nrp, z2);
