@@ -378,12 +378,19 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>())
         a.part[idx * D + d] = v;
         if (d == 0) a.stat[idx] = sh->st_m[h];
     }
+    // the merge kernel may be scheduled once every CTA of this grid got here
+    // or exited; it still waits for this grid's completion before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // out[s][h] = sum_sp part * 2^(m_sp - M) / sum_sp z_sp * 2^(m_sp - M), splits in order.
+// Launched as a programmatic dependent of the split kernel: its launch overlaps
+// the split grid's last CTAs, and it waits here until that grid has completed
+// and its writes are visible.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
     const int32_t L = a.len[s];
     float *o = a.out + ((int64_t)s * a.hq + h) * D;
@@ -532,11 +539,17 @@ cudaError_t launch_decode(const kara_cache *c, int32_t layer, int32_t n, const i
     const dim3 grid((unsigned)a.hkv, (unsigned)n, (unsigned)a.max_splits);
     e = c->head_dim == 128 ? launch_split<128>(km, vm, a, grid, err, st) : launch_split<64>(km, vm, a, grid, err, st);
     if (e != cudaSuccess) return e;
-    if (c->head_dim == 128)
-        decode_combine_kernel<128><<<dim3((unsigned)a.hq, (unsigned)n), 128, 0, st>>>(a);
-    else
-        decode_combine_kernel<64><<<dim3((unsigned)a.hq, (unsigned)n), 64, 0, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.hq, (unsigned)n);
+    cfg.blockDim = dim3((unsigned)c->head_dim);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return c->head_dim == 128 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, a)
+                              : cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, a);
 }
 
 size_t decode_workspace_bytes(const kara_cache *c, int32_t n, int32_t bt_stride)
