@@ -1,6 +1,5 @@
 // Inline-PTX wrappers for sm_100-family features used by the kernels:
-// mbarrier, TMA (cp.async.bulk.tensor, cp.async.bulk), tcgen05 (MMA, TMEM),
-// clusters, DSMEM.
+// mbarrier, TMA (cp.async.bulk.tensor), tcgen05 (MMA, TMEM), clusters, DSMEM.
 // Internal header of the Kara sm_103a library.
 #pragma once
 
@@ -94,23 +93,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// Contiguous global -> shared copy of `bytes` bytes (a multiple of 16; both
-// addresses 16-byte aligned) on the bulk-copy engine; completes `bytes` on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// ---- cp.async (16-byte gathers) ---------------------------------------------
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -178,27 +160,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets its lane's columns.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=r"(v[0]),"=r"(v[1]),"=r"(v[2]),"=r"(v[3]),"=r"(v[4]),"=r"(v[5]),"=r"(v[6]),"=r"(v[7]),"=r"(v[8]),"=r"(v[9]),"=r"(v[10]),"=r"(v[11]),"=r"(v[12]),"=r"(v[13]),"=r"(v[14]),"=r"(v[15]),"=r"(v[16]),"=r"(v[17]),"=r"(v[18]),"=r"(v[19]),"=r"(v[20]),"=r"(v[21]),"=r"(v[22]),"=r"(v[23]),"=r"(v[24]),"=r"(v[25]),"=r"(v[26]),"=r"(v[27]),"=r"(v[28]),"=r"(v[29]),"=r"(v[30]),"=r"(v[31])
-                 : "r"(taddr));
-}
-
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                  : "=r"(v[0]),"=r"(v[1]),"=r"(v[2]),"=r"(v[3]),"=r"(v[4]),"=r"(v[5]),"=r"(v[6]),"=r"(v[7]),"=r"(v[8]),"=r"(v[9]),"=r"(v[10]),"=r"(v[11]),"=r"(v[12]),"=r"(v[13]),"=r"(v[14]),"=r"(v[15])
                  : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                 ::"r"(taddr), "r"(v[0]),"r"(v[1]),"r"(v[2]),"r"(v[3]),"r"(v[4]),"r"(v[5]),"r"(v[6]),"r"(v[7]),"r"(v[8]),"r"(v[9]),"r"(v[10]),"r"(v[11]),"r"(v[12]),"r"(v[13]),"r"(v[14]),"r"(v[15])
-                 : "memory");
 }
 
 // 32 lanes x 8 consecutive 32-bit columns, and the matching store and wait.
@@ -224,56 +191,10 @@ __device__ __forceinline__ void tmem_wait_ld8(uint32_t (&v)[8])
                  : "memory");
 }
 
-// Waits for this thread's 16-column tcgen05.ld results (tied to `v`), with the
-// first 8 values of `w` as operands too, so the instructions producing them are
-// scheduled before the wait.
-__device__ __forceinline__ void tmem_wait_ld16_after(uint32_t (&v)[16], uint32_t (&w)[16])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),
-                 "+r"(w[0]),"+r"(w[1]),"+r"(w[2]),"+r"(w[3]),"+r"(w[4]),"+r"(w[5]),"+r"(w[6]),"+r"(w[7]) : : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]) : : "memory");
-}
-
 // The same wait for two 16-column loads in flight, both register sets tied.
 __device__ __forceinline__ void tmem_wait_ld16x2(uint32_t (&v)[16], uint32_t (&w)[16])
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),
-                 "+r"(w[0]),"+r"(w[1]),"+r"(w[2]),"+r"(w[3]),"+r"(w[4]),"+r"(w[5]),"+r"(w[6]),"+r"(w[7]),"+r"(w[8]),"+r"(w[9]),"+r"(w[10]),"+r"(w[11]),"+r"(w[12]),"+r"(w[13]),"+r"(w[14]),"+r"(w[15]) : : "memory");
-}
-
-// The same wait for two 32-column loads in flight, both register sets tied.
-__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&v)[32], uint32_t (&w)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),"+r"(v[16]),"+r"(v[17]),"+r"(v[18]),"+r"(v[19]),"+r"(v[20]),"+r"(v[21]),"+r"(v[22]),"+r"(v[23]),"+r"(v[24]),"+r"(v[25]),"+r"(v[26]),"+r"(v[27]),"+r"(v[28]),"+r"(v[29]),"+r"(v[30]),"+r"(v[31]),
-                 "+r"(w[0]),"+r"(w[1]),"+r"(w[2]),"+r"(w[3]),"+r"(w[4]),"+r"(w[5]),"+r"(w[6]),"+r"(w[7]),"+r"(w[8]),"+r"(w[9]),"+r"(w[10]),"+r"(w[11]),"+r"(w[12]),"+r"(w[13]),"+r"(w[14]),"+r"(w[15]),"+r"(w[16]),"+r"(w[17]),"+r"(w[18]),"+r"(w[19]),"+r"(w[20]),"+r"(w[21]),"+r"(w[22]),"+r"(w[23]),"+r"(w[24]),"+r"(w[25]),"+r"(w[26]),"+r"(w[27]),"+r"(w[28]),"+r"(w[29]),"+r"(w[30]),"+r"(w[31]) : : "memory");
-}
-
-// Waits for this thread's tcgen05.ld results; `v` is tied to the wait so no use
-// of it can be scheduled before it.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),"+r"(v[16]),"+r"(v[17]),"+r"(v[18]),"+r"(v[19]),"+r"(v[20]),"+r"(v[21]),"+r"(v[22]),"+r"(v[23]),"+r"(v[24]),"+r"(v[25]),"+r"(v[26]),"+r"(v[27]),"+r"(v[28]),"+r"(v[29]),"+r"(v[30]),"+r"(v[31]) : : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns from registers: thread t of the warp
-// writes its lane's columns.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                 ::"r"(taddr), "r"(v[0]),"r"(v[1]),"r"(v[2]),"r"(v[3]),"r"(v[4]),"r"(v[5]),"r"(v[6]),"r"(v[7]),"r"(v[8]),"r"(v[9]),"r"(v[10]),"r"(v[11]),"r"(v[12]),"r"(v[13]),"r"(v[14]),"r"(v[15]),"r"(v[16]),"r"(v[17]),"r"(v[18]),"r"(v[19]),"r"(v[20]),"r"(v[21]),"r"(v[22]),"r"(v[23]),"r"(v[24]),"r"(v[25]),"r"(v[26]),"r"(v[27]),"r"(v[28]),"r"(v[29]),"r"(v[30]),"r"(v[31])
-                 : "memory");
-}
-
-// tcgen05.wait::ld that also takes the first 16 of `w` as operands, so every
-// instruction producing them is scheduled before the wait (the loads it waits
-// for land while those are computed).
-__device__ __forceinline__ void tmem_wait_ld_after(uint32_t (&v)[32], uint32_t (&w)[32])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v[0]),"+r"(v[1]),"+r"(v[2]),"+r"(v[3]),"+r"(v[4]),"+r"(v[5]),"+r"(v[6]),"+r"(v[7]),"+r"(v[8]),"+r"(v[9]),"+r"(v[10]),"+r"(v[11]),"+r"(v[12]),"+r"(v[13]),"+r"(v[14]),"+r"(v[15]),"+r"(v[16]),"+r"(v[17]),"+r"(v[18]),"+r"(v[19]),"+r"(v[20]),"+r"(v[21]),"+r"(v[22]),"+r"(v[23]),"+r"(v[24]),"+r"(v[25]),"+r"(v[26]),"+r"(v[27]),"+r"(v[28]),"+r"(v[29]),"+r"(v[30]),"+r"(v[31]),
                  "+r"(w[0]),"+r"(w[1]),"+r"(w[2]),"+r"(w[3]),"+r"(w[4]),"+r"(w[5]),"+r"(w[6]),"+r"(w[7]),"+r"(w[8]),"+r"(w[9]),"+r"(w[10]),"+r"(w[11]),"+r"(w[12]),"+r"(w[13]),"+r"(w[14]),"+r"(w[15]) : : "memory");
 }
 
@@ -335,32 +256,13 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr)
-{
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// Asynchronous 8-byte store into the shared memory of a CTA of the cluster
-// (`addr` from mapa); completes 8 bytes of transaction count on the mbarrier
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster
+// (`addr` from mapa); completes 4 bytes of transaction count on the mbarrier
 // `bar` (also mapped into that CTA).
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
                  "r"(__float_as_uint(a)), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_f2(uint32_t addr, float a, float b, uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
-                 "f"(a), "f"(b), "r"(bar)
                  : "memory");
 }
 
@@ -377,15 +279,7 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// 1/x on the special-function unit (approximate, flush-to-zero).
-__device__ __forceinline__ float rcp_approx(float x)
-{
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// ---- packed fp32 pairs and 3-input max ----------------------------------------
+// ---- packed fp32 pairs ----------------------------------------------------------
 __device__ __forceinline__ uint64_t pack2(float lo, float hi)
 {
     uint64_t r;
@@ -413,58 +307,8 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
     return d;
 }
 
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c)
-{
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-// ---- 2^y on the FMA pipe ------------------------------------------------------
-// Cody-Waite style split y = n + f, n = round(y), |f| <= 1/2, and
-// 2^y = 2^f * 2^n.  2^f is a degree-4 polynomial whose coefficients come from
-// a Remez exchange that minimises the relative error on [-1/2, 1/2]; evaluated
-// in fp32 Horner form with fused multiply-adds its relative error stays below
-// 3e-6.  2^n is applied by adding n to the exponent field.  Inputs are clamped
-// at -126 so the exponent never underflows (2^-126 stands in for anything
-// smaller, as the flush-to-zero ex2 gives 0 there).  An FMA-pipe alternative
-// to ex2, for the few exponentials of the single-pass scorer's accumulating
-// warps, which would otherwise queue behind the exponential warps' stream on
-// the special-function unit.
-constexpr float kExp2C0 = 0.99999928474426270f;
-constexpr float kExp2C1 = 0.69312179088592530f;
-constexpr float kExp2C2 = 0.24024744331836700f;
-constexpr float kExp2C3 = 0.05591785907745361f;
-constexpr float kExp2C4 = 0.00957010220736265f;
-
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t y2)
-{
-    const uint64_t round_magic = pack2(12582912.f, 12582912.f);  // 1.5 * 2^23
-    float y0, y1;
-    unpack2(y2, y0, y1);
-    const uint64_t y = pack2(fmaxf(y0, -126.f), fmaxf(y1, -126.f));
-    const uint64_t t = add2(y, round_magic);        // n sits in the low mantissa bits of t
-    const uint64_t f = sub2(y, sub2(t, round_magic));
-    uint64_t p = fma2(pack2(kExp2C4, kExp2C4), f, pack2(kExp2C3, kExp2C3));
-    p = fma2(p, f, pack2(kExp2C2, kExp2C2));
-    p = fma2(p, f, pack2(kExp2C1, kExp2C1));
-    p = fma2(p, f, pack2(kExp2C0, kExp2C0));
-    float p0, p1, t0, t1;
-    unpack2(p, p0, p1);
-    unpack2(t, t0, t1);
-    const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-    const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
-    return pack2(r0, r1);
-}
-
-// 1/x on the FMA pipe, for x in [2^-120, 2^120]: the exponent-flip guess
+// ---- reciprocal on the FMA pipe ------------------------------------------------
+// 1/x for x in [2^-120, 2^120]: the exponent-flip guess
 // 2^127 / x read off the bit pattern (0x7F000000 - bits(x), relative error at
 // most 1/8) and three Newton steps y <- y (2 - x y), each squaring the error
 // (1/8 -> 2^-6 -> 2^-12 -> 2^-24, plus rounding).
@@ -475,14 +319,6 @@ __device__ __forceinline__ float rcp_newton(float x)
     y = y * fmaf(-x, y, 2.f);
     y = y * fmaf(-x, y, 2.f);
     return y;
-}
-
-// Scalar form of exp2_poly2 (same coefficients and steps).
-__device__ __forceinline__ float exp2_poly(float y)
-{
-    float lo, hi;
-    unpack2(exp2_poly2(pack2(y, y)), lo, hi);
-    return lo;
 }
 
 }  // namespace ptx
