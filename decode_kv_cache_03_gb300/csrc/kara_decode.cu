@@ -25,11 +25,11 @@
 // The weights P are fp32; each enters the second product as the sum of two
 // bf16 terms (hi = rn(p), lo = rn(p - hi)), so its relative error is about
 // 2^-17, as good as the fp32 sums around it.  The tensor cores here only
-// save issue slots: about 4 warp instructions per key instead of 46 on the
-// CUDA cores, which left the consumers, not HBM, as the limit.  Between the
-// two products, the softmax of the split runs in shared memory.  A second
-// kernel combines the splits of each (sequence, head) in a fixed order, so
-// the result is deterministic.
+// save issue slots: on the CUDA cores the same work took about 46 warp
+// instructions per key and the consumers, not HBM, set the pace; here it
+// takes about 4.  Between the two products, the softmax of the split runs in
+// shared memory.  A second kernel combines the splits of each (sequence, head)
+// in a fixed order, so the result is deterministic.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
