@@ -172,3 +172,47 @@ def test_decode_reads_a_bad_block_as_zeros():
                               wl.bt_stride, wl.num_blocks + 1)
     ref = oracle.decode_attention(shape, 0, q, kz, vz, bt_ref, wl.lengths)
     np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
+
+
+def _decode_inputs(seed, n, hkv, G, D, nblk):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(1, nblk, hkv, 16, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, nblk, hkv, 16, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(n, G * hkv, D, generator=g).to(torch.bfloat16)
+    return k, v, q
+
+
+def test_decode_at_the_sequence_limit():
+    """n = 65535 sequences (the largest batch a call takes), one block of 1..16
+    keys each, block ids shuffled: every output against the oracle."""
+    kara = lib()
+    n, hkv, G, D = 65535, 1, 2, 64
+    k, v, q = _decode_inputs(41, n, hkv, G, D, n)
+    g = torch.Generator().manual_seed(42)
+    lengths = torch.randint(1, 17, (n,), generator=g, dtype=torch.int32)
+    bt = torch.randperm(n, generator=g).to(torch.int32).reshape(n, 1)
+    got, st = run_decode(kara, k.cuda(), v.cuda(), G * hkv, 0, lengths.cuda(), bt.cuda(), q.cuda())
+    assert st == 0
+    sh = oracle.make_shape(n, 1, G * hkv, hkv, D, 16, 64, 16, 8, 16, 0.1, 1, n)
+    ref = oracle.decode_attention(sh, 0, q, k, v, bt, lengths)
+    np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
+
+
+def test_decode_long_sequence_of_repeated_blocks():
+    """One sequence of 4096 * 1024 keys (4096 splits) whose table cycles through
+    the same 64 blocks: every key occurs equally often, so the exact result is
+    the decode over those 1024 distinct keys once (oracle on a 64-block table)."""
+    kara = lib()
+    hkv, G, D, nblk = 2, 4, 128, 64
+    splits = 4096
+    L = splits * 1024
+    k, v, q = _decode_inputs(43, 1, hkv, G, D, nblk)
+    g = torch.Generator().manual_seed(44)
+    cycle = torch.randperm(nblk, generator=g).to(torch.int32)
+    bt = cycle.repeat(splits).reshape(1, splits * nblk)
+    lengths = torch.tensor([L], dtype=torch.int32)
+    got, st = run_decode(kara, k.cuda(), v.cuda(), G * hkv, 0, lengths.cuda(), bt.cuda(), q.cuda())
+    assert st == 0
+    sh = oracle.make_shape(1, 1, G * hkv, hkv, D, 16, 64, 16, 8, 16, 0.1, nblk, nblk)
+    ref = oracle.decode_attention(sh, 0, q, k, v, cycle.reshape(1, nblk), torch.tensor([1024], dtype=torch.int32))
+    np.testing.assert_allclose(got, ref, atol=ATOL, rtol=RTOL)
