@@ -184,6 +184,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>())
     float *logit = reinterpret_cast<float *>(ring + kStages * BB);  // [G][kLs]
     DecShared *sh = reinterpret_cast<DecShared *>(logit + G * kLs);
 
+    // launched as a programmatic dependent of whatever precedes it on the
+    // stream (the previous call's merge, or the compaction that rewrote the
+    // table): nothing global is read before that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int sp = blockIdx.z, g = blockIdx.x, s = blockIdx.y;
     const int32_t L = a.len[s];
     if (!length_ok(a, L)) {
@@ -386,7 +390,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, G>())
 // out[s][h] = sum_sp part * 2^(m_sp - M) / sum_sp z_sp * 2^(m_sp - M), splits in order.
 // Launched as a programmatic dependent of the split kernel: its launch overlaps
 // the split grid's last CTAs, and it waits here until that grid has completed
-// and its writes are visible.
+// and its writes are visible.  It lets the next call's split kernel launch as
+// it finishes.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a)
 {
@@ -410,6 +415,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a)
         num = fmaf(a.part[(base + sp) * D + d], w, num);
     }
     o[d] = num / den;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Tensor map over one pool, (d, slot, kv head, block, layer) with the cache's
@@ -478,8 +484,17 @@ cudaError_t launch_split_g(const CUtensorMap &km, const CUtensorMap &vm, const D
     auto kern = decode_split_kernel<D, G>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecThreads, smem, st>>>(km, vm, a, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, km, vm, a, err);
 }
 
 template <int D>

@@ -210,8 +210,10 @@ kara_status kara_append_queries(const kara_cache *c, const kara_params *p, const
  * that runs out records KARA_ETIMEOUT (outputs are then unspecified).
  * Returns KARA_ECUDA, before any launch, if the TMA tensor map over a pool
  * cannot be encoded (a stride of 2^40 bytes or more, for one).
- * Two launches on `stream` (the splits, then their merge as a programmatic
- * dependent); the call may be captured into a CUDA graph.
+ * Two launches on `stream`, both programmatic dependents of what precedes
+ * them (the splits wait for the stream's previous kernel to complete before
+ * reading anything; the merge waits for the splits); the call may be captured
+ * into a CUDA graph.
  * Layout: each (block, KV head) slice of a pool must be block_size * head_dim
  * contiguous bf16 (rows at stride head_dim), as in the layout above.
  * Supported: the kara_cache shapes above; n <= 65535; bt_stride * block_size up to
