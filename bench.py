@@ -261,6 +261,9 @@ def dist_setup():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
+        if torch.cuda.is_available():
+            # each rank's GPU is bound before NCCL sets up its communicator
+            torch.cuda.set_device(local)
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend)
     return ws, rank, local
