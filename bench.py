@@ -62,22 +62,34 @@ def exp_diagnostic(spec, nwin, causal, score_ms, mhz, n_sm):
     return out
 
 
-def measured_traffic(nwin):
-    """DRAM bytes of one scoring launch from the committed ncu capture, scaled by
-    windows; None when the scorer's sources changed since the capture."""
+def traffic_record(name):
+    """A committed ncu traffic record under profiles/, or None when the sources
+    it was taken from have changed since the capture."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "score_sp_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             rec = json.load(f)
         h = hashlib.sha256()
         for src in rec["sources"]:
             with open(os.path.join(ROOT, src), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest()[:16] != rec["sources_sha256_16"]:
-            return None
-        return rec["bytes_per_window"] * nwin
+        return rec if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
     except Exception:
         return None
+
+
+def measured_traffic(nwin):
+    """DRAM bytes of one scoring launch from the committed ncu capture, scaled by
+    windows; None when the scorer's sources changed since the capture."""
+    rec = traffic_record("score_sp_traffic.json")
+    return rec["bytes_per_window"] * nwin if rec else None
+
+
+def measured_decode_traffic(kv_bytes):
+    """DRAM bytes of one decode split launch from the committed ncu capture,
+    scaled by the launch's K/V bytes; None when the sources changed since."""
+    rec = traffic_record("decode_split_traffic.json")
+    return round(rec["dram_bytes"] / rec["kv_bytes_captured"] * kv_bytes) if rec else None
 
 
 def algorithmic(spec, lengths):
@@ -682,7 +694,10 @@ def run_decode(args, dev, kara):
             "config": {"workload": f"{args.config}, one layer: {n} sequences x {spec.hq} query / {spec.hkv} KV heads, "
                                    f"D {spec.d}, lengths {spec.len_lo}..{spec.len_hi}, {kv_bytes / 1e9:.2f} GB of K/V",
                        "l2": "K/V larger than L2, every block distinct"},
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk, "unit": "GB/s", "frac": gbs / pk},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk, "unit": "GB/s", "frac": gbs / pk,
+                         "traffic": measured_decode_traffic(kv_bytes),
+                         "traffic_unit": "bytes per launch of the split kernel (DRAM read + write)",
+                         "algorithmic_bytes": kv_bytes + io_bytes},
             "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
